@@ -1,0 +1,188 @@
+"""CPU oracle for the packed varlen causal depthwise conv1d (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never touches it, and it never touches the product path.
+
+The arithmetic lives in ``kda_conv_ref.c`` (plain single-threaded C, FP32 as
+the vLLM page "vllm.models.kimi_k3.nvidia.ops.kda_conv" fixes it: module
+docstring, 3rd and 4th paragraphs, and the packed_causal_conv1d_fn docstring).
+This module compiles it with gcc and marshals numpy arrays into it.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_conv_ref.c")
+_LIB_PATH = os.path.join(_HERE, "libkda_conv_ref.so")
+_lock = threading.Lock()
+_lib = None
+
+REF_OK = 0
+REF_BAD_SHAPE = 1
+REF_BAD_QSL = 2
+REF_BAD_CACHE_INDEX = 3
+REF_DUP_CACHE_INDEX = 4
+
+# No contraction of a*b+c into FMA behind the source's back: every fused
+# multiply-add in the oracle is an explicit fmaf().
+CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compiles the oracle into a shared library and returns its path."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, src, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    lib.kda_ref_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.kda_ref_bf16_to_f32.restype = ctypes.c_float
+    lib.kda_ref_bf16_rne.argtypes = [ctypes.c_float]
+    lib.kda_ref_bf16_rne.restype = ctypes.c_uint16
+    lib.kda_ref_silu.argtypes = [ctypes.c_float]
+    lib.kda_ref_silu.restype = ctypes.c_float
+    for name in ("kda_ref_bf16_to_f32_n", "kda_ref_bf16_rne_n", "kda_ref_silu_n"):
+        getattr(lib, name).argtypes = [P, I64, P]
+        getattr(lib, name).restype = None
+    lib.kda_ref_silu_bf16_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, P]
+    lib.kda_ref_silu_bf16_range.restype = None
+    lib.kda_ref_check_metadata.argtypes = [I64, I64, P, P, I64, I64, ctypes.POINTER(I64)]
+    lib.kda_ref_check_metadata.restype = ctypes.c_int
+    lib.kda_ref_packed_conv1d.argtypes = [
+        P, I64, I64, I64, I64,  # x, x_row_stride, tokens, dim, part_dim
+        P, P, P, I64,  # weight, bias, conv_states, cache_lines
+        P, P, P, I64, I64,  # cache_indices, has_initial_state, qsl, num_seqs, null_block_id
+        ctypes.c_int, P, P, P,  # activation, out, preact, act
+    ]
+    lib.kda_ref_packed_conv1d.restype = ctypes.c_int
+    return lib
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Returns the oracle library, building it on first use."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _ptr(a: np.ndarray | None) -> int | None:
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def bf16_to_f32(bits: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Widens bf16 bit patterns (uint16) to fp32, elementwise, via the oracle."""
+    lib = lib or load()
+    flat = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
+    out = np.empty(flat.size, dtype=np.float32)
+    lib.kda_ref_bf16_to_f32_n(flat.ctypes.data, flat.size, out.ctypes.data)
+    return out.reshape(np.shape(bits))
+
+
+def bf16_rne(values: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Rounds fp32 values to bf16 bit patterns (uint16), elementwise, via the oracle."""
+    lib = lib or load()
+    flat = np.ascontiguousarray(values, dtype=np.float32).ravel()
+    out = np.empty(flat.size, dtype=np.uint16)
+    lib.kda_ref_bf16_rne_n(flat.ctypes.data, flat.size, out.ctypes.data)
+    return out.reshape(np.shape(values))
+
+
+def silu(values: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """SiLU in fp32, elementwise, via the oracle."""
+    lib = lib or load()
+    flat = np.ascontiguousarray(values, dtype=np.float32).ravel()
+    out = np.empty(flat.size, dtype=np.float32)
+    lib.kda_ref_silu_n(flat.ctypes.data, flat.size, out.ctypes.data)
+    return out.reshape(np.shape(values))
+
+
+def silu_bf16_range(first: int, count: int, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """bf16_rne(silu(f)) for the fp32 bit patterns first .. first+count-1."""
+    lib = lib or load()
+    out = np.empty(count, dtype=np.uint16)
+    lib.kda_ref_silu_bf16_range(first, count, out.ctypes.data)
+    return out
+
+
+def check_metadata(tokens, cache_lines, cache_indices, query_start_loc, null_block_id,
+                   lib: ctypes.CDLL | None = None) -> tuple[int, int]:
+    """(status, offending sequence index or -1) for one call's metadata."""
+    lib = lib or load()
+    ci = np.ascontiguousarray(cache_indices, dtype=np.int32)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    bad = ctypes.c_int64(-1)
+    rc = lib.kda_ref_check_metadata(tokens, cache_lines, _ptr(ci), _ptr(qsl), qsl.size - 1,
+                                    null_block_id, ctypes.byref(bad))
+    return rc, bad.value
+
+
+def packed_conv1d(x_bits: np.ndarray, col_offset: int, dim: int, part_dim: int,
+                  weight: np.ndarray,
+                  bias: np.ndarray | None, conv_states: np.ndarray, cache_indices: np.ndarray,
+                  has_initial_state: np.ndarray, query_start_loc: np.ndarray,
+                  null_block_id: int, activation: int, out: np.ndarray | None = None,
+                  want_preact: bool = False, want_act: bool = False,
+                  lib: ctypes.CDLL | None = None) -> dict:
+    """Runs the oracle conv.
+
+    ``x_bits`` is a (tokens, row_stride) uint16 array of bf16 bits (the whole
+    in_proj buffer); the input is its columns [col_offset, col_offset + dim).
+    ``conv_states`` (cache_lines, dim, 3) float32 is updated in place.  ``out``
+    (dim/part_dim, tokens, part_dim) uint16, if given, is written in place
+    (rows outside the sequences keep their contents); otherwise a fresh array
+    filled with 0xFFFF is used.  Returns a dict with ``out`` and, on request,
+    ``preact`` / ``act`` (float32, same layout, NaN where not written).
+    """
+    lib = lib or load()
+    assert x_bits.dtype == np.uint16 and x_bits.ndim == 2
+    assert x_bits.flags["C_CONTIGUOUS"]
+    tokens, row_stride = x_bits.shape
+    assert 0 <= col_offset and col_offset + dim <= row_stride
+    assert conv_states.dtype == np.float32 and conv_states.flags["C_CONTIGUOUS"]
+    assert conv_states.ndim == 3 and conv_states.shape[1:] == (dim, 3)
+    weight = np.ascontiguousarray(weight, dtype=np.float32)
+    bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    ci = np.ascontiguousarray(cache_indices, dtype=np.int32)
+    his = np.ascontiguousarray(has_initial_state, dtype=np.uint8)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    num_seqs = qsl.size - 1
+    planes = dim // part_dim if part_dim > 0 else 0
+    if out is None:
+        out = np.full((planes, tokens, part_dim), 0xFFFF, dtype=np.uint16)
+    assert out.dtype == np.uint16 and out.flags["C_CONTIGUOUS"]
+    preact = np.full(out.shape, np.nan, dtype=np.float32) if want_preact else None
+    act = np.full(out.shape, np.nan, dtype=np.float32) if want_act else None
+    rc = lib.kda_ref_packed_conv1d(
+        x_bits.ctypes.data + 2 * col_offset, row_stride, tokens, dim, part_dim,
+        _ptr(weight), _ptr(bias), _ptr(conv_states), conv_states.shape[0],
+        _ptr(ci), _ptr(his), _ptr(qsl), num_seqs, null_block_id,
+        activation, _ptr(out), _ptr(preact), _ptr(act))
+    if rc != REF_OK:
+        raise ValueError(f"oracle rejected the call: status {rc}")
+    res = {"out": out}
+    if want_preact:
+        res["preact"] = preact
+    if want_act:
+        res["act"] = act
+    return res

@@ -1,0 +1,223 @@
+/*
+ * Test oracle for the packed varlen causal depthwise conv1d of the Kimi-K3 KDA
+ * layer.  TEST INFRASTRUCTURE ONLY: the product path never links, loads or
+ * calls this file; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark do.
+ *
+ * Plain, slow, single-threaded C.  It shares no code with the CUDA path.
+ * Every number is computed the obvious way: one sequence, one channel, one
+ * token at a time.
+ *
+ * What it computes follows "vllm.models.kimi_k3.nvidia.ops.kda_conv"
+ * (docs.vllm.ai, module docstring and packed_causal_conv1d_fn):
+ *   - module docstring, 3rd paragraph: bf16 input is widened to FP32 exactly,
+ *     the taps use FP32 weights and an FP32 conv state, then SiLU, then the
+ *     FP32 result is rounded to bf16 to nearest even and stored as dense
+ *     (tokens, part_dim) planes, one per part;
+ *   - module docstring, 4th paragraph: a sequence's conv state is read once
+ *     and the updated state (the last 3 input rows) is written back;
+ *   - packed_causal_conv1d_fn docstring: width-4 causal depthwise conv with
+ *     the semantics of causal_conv1d_fn(x.T, ...).T, conv_states of shape
+ *     (cache lines, dim, 3) updated in place, output (dim/part_dim, tokens,
+ *     part_dim), plane i holding channels [i*part_dim, (i+1)*part_dim).
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes): the accumulator starts at bias[c] (+0.0f without bias) and the four
+ * products are added with fused multiply-adds, oldest tap first; SiLU is
+ * a / (1 + exp(-a)) in FP32; conv state index 2 is the most recent row;
+ * a sequence whose cache index equals null_block_id is computed with a zero
+ * history and its state is neither read nor written; token rows outside
+ * [query_start_loc[0], query_start_loc[num_seqs]) are not written.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC (no FMA
+ * contraction: every fused multiply-add below is an explicit fmaf call).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* Status codes returned by the oracle (not the library's codes). */
+#define REF_OK 0
+#define REF_BAD_SHAPE 1
+#define REF_BAD_QSL 2
+#define REF_BAD_CACHE_INDEX 3
+#define REF_DUP_CACHE_INDEX 4
+
+static float f32_from_bits(uint32_t u) {
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint32_t bits_from_f32(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+
+/* bf16 -> fp32: a bf16 value is the upper half of an fp32 bit pattern, so the
+ * widening is exact (module docstring: "bf16 -> FP32 is exact"). */
+float kda_ref_bf16_to_f32(uint16_t h) { return f32_from_bits((uint32_t)h << 16); }
+
+/* fp32 -> bf16, round to nearest, ties to even, from the definition: keep the
+ * upper 16 bits and round on the lower 16.  A carry out of the mantissa bumps
+ * the exponent, which is what rounding up across a binade (or to infinity)
+ * means.  A NaN stays a NaN with its sign: the quiet bit is set so that
+ * truncating a payload that lives only in the lower half cannot make it an
+ * infinity. */
+uint16_t kda_ref_bf16_rne(float f) {
+    uint32_t u = bits_from_f32(f);
+    uint32_t hi = u >> 16;
+    uint32_t lo = u & 0xFFFFu;
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) {
+        return (uint16_t)(hi | 0x0040u);
+    }
+    if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) {
+        hi += 1u;
+    }
+    return (uint16_t)hi;
+}
+
+/* SiLU(a) = a * sigmoid(a) = a / (1 + exp(-a)), all in FP32. */
+float kda_ref_silu(float a) {
+    float e = expf(-a);
+    float d = 1.0f + e;
+    return a / d;
+}
+
+/* Elementwise array forms of the three functions above. */
+void kda_ref_bf16_to_f32_n(const uint16_t *in, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kda_ref_bf16_to_f32(in[i]);
+}
+
+void kda_ref_bf16_rne_n(const float *in, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kda_ref_bf16_rne(in[i]);
+}
+
+void kda_ref_silu_n(const float *in, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kda_ref_silu(in[i]);
+}
+
+/* bf16_rne(silu(f)) for `count` consecutive fp32 bit patterns starting at
+ * `first`.  Used to check a device epilogue over the whole fp32 range. */
+void kda_ref_silu_bf16_range(uint32_t first, uint64_t count, uint16_t *out) {
+    for (uint64_t i = 0; i < count; ++i) {
+        float a = f32_from_bits((uint32_t)(first + i));
+        out[i] = kda_ref_bf16_rne(kda_ref_silu(a));
+    }
+}
+
+/* Checks the metadata of one call.  On failure *bad_index is the offending
+ * sequence index (or -1).  Returns a REF_* code. */
+int kda_ref_check_metadata(int64_t tokens, int64_t cache_lines, const int32_t *cache_indices,
+                           const int32_t *query_start_loc, int64_t num_seqs,
+                           int64_t null_block_id, int64_t *bad_index) {
+    *bad_index = -1;
+    if (tokens < 0 || num_seqs < 0 || cache_lines < 0) return REF_BAD_SHAPE;
+    if (num_seqs == 0) return REF_OK;
+    if (query_start_loc[0] < 0) {
+        *bad_index = 0;
+        return REF_BAD_QSL;
+    }
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        if (query_start_loc[s + 1] < query_start_loc[s]) {
+            *bad_index = s;
+            return REF_BAD_QSL;
+        }
+    }
+    if ((int64_t)query_start_loc[num_seqs] > tokens) {
+        *bad_index = num_seqs;
+        return REF_BAD_QSL;
+    }
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        int64_t line = cache_indices[s];
+        if (line == null_block_id) continue;
+        if (line < 0 || line >= cache_lines) {
+            *bad_index = s;
+            return REF_BAD_CACHE_INDEX;
+        }
+        for (int64_t r = 0; r < s; ++r) {
+            if ((int64_t)cache_indices[r] == line) {
+                *bad_index = s;
+                return REF_DUP_CACHE_INDEX;
+            }
+        }
+    }
+    return REF_OK;
+}
+
+/*
+ * The conv, one call.
+ *
+ * x           bf16 bits, token row t at x[t * x_row_stride], dim channels used.
+ * weight      (dim, 4) fp32, weight[c*4 + j] multiplies row t-3+j.
+ * bias        (dim) fp32 or NULL.
+ * conv_states (cache_lines, dim, 3) fp32, updated in place.
+ * out         (dim/part_dim, tokens, part_dim) bf16 bits.
+ * preact      NULL or (dim/part_dim, tokens, part_dim) fp32: the accumulator
+ *             before the activation.
+ * act         NULL or the same layout: the fp32 value after the activation,
+ *             before rounding.
+ * activation  0 = none, 1 = SiLU.
+ */
+int kda_ref_packed_conv1d(const uint16_t *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
+                          int64_t part_dim, const float *weight, const float *bias,
+                          float *conv_states, int64_t cache_lines, const int32_t *cache_indices,
+                          const uint8_t *has_initial_state, const int32_t *query_start_loc,
+                          int64_t num_seqs, int64_t null_block_id, int activation, uint16_t *out,
+                          float *preact, float *act) {
+    int64_t bad;
+    if (tokens < 0 || dim < 0 || part_dim <= 0 || num_seqs < 0) return REF_BAD_SHAPE;
+    if (dim % part_dim != 0 || x_row_stride < dim) return REF_BAD_SHAPE;
+    if (activation != 0 && activation != 1) return REF_BAD_SHAPE;
+    if (tokens == 0 || num_seqs == 0) return REF_OK;
+    int rc = kda_ref_check_metadata(tokens, cache_lines, cache_indices, query_start_loc, num_seqs,
+                                    null_block_id, &bad);
+    if (rc != REF_OK) return rc;
+
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        int64_t a = query_start_loc[s];
+        int64_t len = (int64_t)query_start_loc[s + 1] - a;
+        if (len <= 0) continue; /* an empty sequence: no output, state untouched */
+        int64_t line = cache_indices[s];
+        int is_null = (line == null_block_id);
+        int read_state = !is_null && has_initial_state[s];
+
+        for (int64_t c = 0; c < dim; ++c) {
+            /* History rows -3, -2, -1 of the sequence: h[0] oldest, h[2] newest. */
+            float h[3] = {0.0f, 0.0f, 0.0f};
+            if (read_state) {
+                for (int k = 0; k < 3; ++k) h[k] = conv_states[(line * dim + c) * 3 + k];
+            }
+            int64_t plane = c / part_dim;
+            int64_t col = c % part_dim;
+
+            for (int64_t t = 0; t < len; ++t) {
+                float acc = bias ? bias[c] : 0.0f;
+                for (int j = 0; j < 4; ++j) {
+                    int64_t r = t - 3 + j; /* sequence-relative row of tap j */
+                    float v = (r >= 0) ? kda_ref_bf16_to_f32(x[(a + r) * x_row_stride + c])
+                                       : h[r + 3];
+                    acc = fmaf(v, weight[c * 4 + j], acc);
+                }
+                float y = activation ? kda_ref_silu(acc) : acc;
+                int64_t o = (plane * tokens + (a + t)) * part_dim + col;
+                out[o] = kda_ref_bf16_rne(y);
+                if (preact) preact[o] = acc;
+                if (act) act[o] = y;
+            }
+
+            if (!is_null) {
+                /* New state: the last 3 rows of [h ; x rows of the sequence]. */
+                float ns[3];
+                for (int k = 0; k < 3; ++k) {
+                    int64_t r = len - 3 + k;
+                    ns[k] = (r >= 0) ? kda_ref_bf16_to_f32(x[(a + r) * x_row_stride + c])
+                                     : h[r + 3];
+                }
+                for (int k = 0; k < 3; ++k) conv_states[(line * dim + c) * 3 + k] = ns[k];
+            }
+        }
+    }
+    return REF_OK;
+}

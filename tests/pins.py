@@ -1,0 +1,500 @@
+"""Independent checks that pin the CPU oracle to the pages and to mathematics.
+
+Each ``pin_*`` function takes an oracle library handle (so that the same
+checks can be run against deliberately broken copies of the oracle) and
+raises AssertionError on a mismatch.  None of them re-types the oracle's
+loop: they use a different formulation (a materialised padded column per
+(sequence, channel) and exact rational arithmetic), a library routine
+(torch's float64 conv1d and silu, torch's bf16 conversions), a closed form,
+or an invariant that any correct implementation must satisfy.
+
+What they follow: "vllm.models.kimi_k3.nvidia.ops.kda_conv" (docs.vllm.ai),
+module docstring (exact bf16 widening, FP32 taps with FP32 weights and
+state, SiLU, round to nearest even, dense planes; the state read once and
+written back) and the packed_causal_conv1d_fn docstring (width-4 causal
+depthwise conv as causal_conv1d_fn(x.T, ...).T, conv_states (lines, dim, 3)
+updated in place, output (dim/part_dim, tokens, part_dim)).
+"""
+
+from __future__ import annotations
+
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+
+U = 2.0 ** -24  # unit roundoff of fp32
+
+
+# --------------------------------------------------------------------------
+# Library conversions (torch CPU) used as independent references
+# --------------------------------------------------------------------------
+
+def torch_bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).float().numpy()
+
+
+def torch_f32_to_bf16(vals: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(vals, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def is_nan_bf16(bits: np.ndarray) -> np.ndarray:
+    bits = np.asarray(bits, dtype=np.uint16)
+    return ((bits & 0x7F80) == 0x7F80) & ((bits & 0x007F) != 0)
+
+
+# --------------------------------------------------------------------------
+# Exact rational fp32 arithmetic
+# --------------------------------------------------------------------------
+
+_F32_MAX = Fraction((2 ** 24 - 1) * 2 ** 104)
+
+
+def round_to_f32(q: Fraction) -> float:
+    """Nearest fp32 to the exact rational q, ties to even (q != 0)."""
+    sign = -1.0 if q < 0 else 1.0
+    a = -q if q < 0 else q
+    # e with 2^e <= a < 2^(e+1)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if (Fraction(2) ** e) > a:
+        e -= 1
+    e = max(e, -126)  # below the normal range the quantum stays 2^-149
+    qe = e - 23
+    m = a / (Fraction(2) ** qe)
+    n = m.numerator // m.denominator
+    r = m - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    v = Fraction(n) * (Fraction(2) ** qe)
+    if v > _F32_MAX:
+        return sign * float("inf")
+    return sign * float(v)
+
+
+def fma_f32(a: float, b: float, c: float) -> float:
+    """fp32 fused multiply-add of fp32-valued floats, one rounding, exact rationals."""
+    exact = Fraction(a) * Fraction(b) + Fraction(c)
+    if exact == 0:
+        prod_neg = (np.signbit(a) != np.signbit(b))
+        prod_zero = (a == 0.0 or b == 0.0)
+        if prod_zero and c == 0.0 and prod_neg and np.signbit(c):
+            return -0.0
+        return 0.0
+    return round_to_f32(exact)
+
+
+# --------------------------------------------------------------------------
+# Second formulation of the conv: a padded column per (sequence, channel)
+# --------------------------------------------------------------------------
+
+def padded_columns(b: workloads.Batch, s: int) -> tuple[np.ndarray, bool]:
+    """(L+3, dim) float64 column [h0, h1, h2, x_a, ..., x_{a+L-1}] of sequence s
+    (history rows first, oldest first) and whether its state line is live."""
+    a, e = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+    line = int(b.cache_indices[s])
+    live = line != b.null_block_id
+    hist = np.zeros((3, b.dim), dtype=np.float64)
+    if live and b.has_initial_state[s]:
+        hist = b.conv_states[line].T.astype(np.float64)  # (3, dim): row k = state index k
+    xs = torch_bf16_to_f32(b.x_buf[a:e, b.col_offset:b.col_offset + b.dim]).astype(np.float64)
+    return np.concatenate([hist, xs], axis=0), live
+
+
+def run_oracle(b: workloads.Batch, lib=None, **kw) -> dict:
+    return oracle.packed_conv1d(
+        b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, b.conv_states,
+        b.cache_indices, b.has_initial_state, b.query_start_loc, b.null_block_id,
+        b.activation, lib=lib, **kw)
+
+
+def plane_view(arr: np.ndarray, b: workloads.Batch) -> np.ndarray:
+    """(planes, tokens, part_dim) -> (tokens, dim) with channel c at column c."""
+    planes, tokens, p = arr.shape
+    return np.ascontiguousarray(arr.transpose(1, 0, 2).reshape(tokens, planes * p))
+
+
+def small_batch(seed: int, lengths, dim=128, part_dim=64, row_stride=None, col_offset=8,
+                cache_lines=None, null_count=1, his_p=0.6, activation=1, bias=True,
+                tokens=None, first_token=0, x_std=1.0, w_range=0.5) -> workloads.Batch:
+    n = len(lengths)
+    row_stride = row_stride or (dim + 24)
+    cache_lines = cache_lines or (n + 3)
+    return workloads.make_batch(
+        f"small{seed}", seed, lengths, dim, part_dim, row_stride, cache_lines,
+        col_offset=col_offset, x_std=x_std, w_range=w_range,
+        bias_std=0.1 if bias else None, activation=activation, his_p=his_p,
+        null_count=null_count, tokens=tokens, first_token=first_token)
+
+
+# --------------------------------------------------------------------------
+# Pins
+# --------------------------------------------------------------------------
+
+def pin_bf16_widen(lib) -> None:
+    """Every bf16 pattern widens to the value torch's conversion gives, and
+    rounds back to itself (NaNs: stay NaN)."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.bf16_to_f32(allb, lib)
+    want = torch_bf16_to_f32(allb)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+    back = oracle.bf16_rne(got, lib)
+    assert np.array_equal(back[~nan], allb[~nan])
+    assert is_nan_bf16(back[nan]).all()
+
+
+RNE_CASES = [  # (fp32 bits, bf16 bits) worked from the definition of round-half-even
+    (0x3F808000, 0x3F80),  # tie, even below
+    (0x3F818000, 0x3F82),  # tie, odd below -> up
+    (0x3F808001, 0x3F81),  # just above the tie
+    (0x3F807FFF, 0x3F80),  # just below the tie
+    (0xBF808000, 0xBF80),  # negative tie, even
+    (0xBF818000, 0xBF82),  # negative tie, odd
+    (0x3FFF8000, 0x4000),  # tie that carries into the exponent
+    (0x7F7FFFFF, 0x7F80),  # largest finite fp32 rounds to +inf
+    (0x7F7F7FFF, 0x7F7F),  # stays finite
+    (0x00008000, 0x0000),  # subnormal tie to even zero
+    (0x00018000, 0x0002),  # subnormal tie up
+    (0x80000000, 0x8000),  # -0
+    (0x7F800000, 0x7F80),  # +inf
+    (0xFF800000, 0xFF80),  # -inf
+]
+
+
+def pin_bf16_rne(lib, n_random: int = 1 << 20, seed: int = 7) -> None:
+    """Hand-worked ties, then random patterns against torch's RNE conversion."""
+    src = np.array([c[0] for c in RNE_CASES], dtype=np.uint32).view(np.float32)
+    want = np.array([c[1] for c in RNE_CASES], dtype=np.uint16)
+    got = oracle.bf16_rne(src, lib)
+    assert np.array_equal(got, want), [hex(v) for v in got]
+    rng = np.random.default_rng(seed)
+    pats = rng.integers(0, 2 ** 32, size=n_random, dtype=np.uint64).astype(np.uint32)
+    vals = pats.view(np.float32)
+    got = oracle.bf16_rne(vals, lib)
+    ref = torch_f32_to_bf16(vals)
+    nan = np.isnan(vals)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert is_nan_bf16(got[nan]).all()
+    # NaN keeps its sign.
+    assert np.array_equal(got[nan] >> 15, (pats[nan] >> 31).astype(np.uint16))
+
+
+def _check_against_columns(b: workloads.Batch, res: dict, states_after: np.ndarray,
+                           exact: bool) -> None:
+    """Compares the oracle's preact / states with the padded-column formulation.
+
+    exact=True: the fp32 chain acc=bias; acc=fma(v_j, w_j, acc), j oldest
+    first, evaluated in exact rationals with one rounding per step; must be
+    bit-identical.  exact=False: float64 window dot products within the
+    error bound of four fp32 roundings."""
+    pre = plane_view(res["preact"], b)
+    w = b.weight.astype(np.float64)
+    bias = np.zeros(b.dim) if b.bias is None else b.bias.astype(np.float64)
+    expected_states = b.conv_states.copy()
+    for s in range(b.num_seqs):
+        a, e = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+        L = e - a
+        if L <= 0:
+            continue
+        col, live = padded_columns(b, s)
+        if live:
+            expected_states[int(b.cache_indices[s])] = col[L:L + 3].T.astype(np.float32)
+        for t in range(L):
+            win = col[t:t + 4]  # (4, dim), oldest first
+            got = pre[a + t]
+            if exact:
+                for c in range(b.dim):
+                    acc = float(np.float32(bias[c])) if b.bias is not None else 0.0
+                    for j in range(4):
+                        acc = fma_f32(float(win[j, c]), float(w[c, j]), acc)
+                    assert np.float32(acc).view(np.uint32) == np.float32(got[c]).view(np.uint32), \
+                        (s, t, c, acc, got[c])
+            else:
+                ref = bias + (win * w.T).sum(axis=0)
+                mag = np.abs(bias) + (np.abs(win) * np.abs(w.T)).sum(axis=0)
+                err = np.abs(got.astype(np.float64) - ref)
+                assert (err <= 4 * U * mag + 1e-40).all(), (s, t, float(err.max()))
+    assert np.array_equal(states_after.view(np.uint32), expected_states.view(np.uint32))
+
+
+def pin_exact_rational(lib) -> None:
+    """Brute force on tiny inputs: bit-identical pre-activations and states."""
+    for seed, lengths in [(11, [1, 2, 3, 4, 5]), (12, [7, 0, 3, 9]), (13, [6, 2, 1, 5, 4])]:
+        b = small_batch(seed, lengths, dim=64, part_dim=64, null_count=1)
+        st = b.conv_states.copy()
+        res = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias,
+                                   st, b.cache_indices, b.has_initial_state, b.query_start_loc,
+                                   b.null_block_id, b.activation, want_preact=True, lib=lib)
+        _check_against_columns(b, res, st, exact=True)
+    b = small_batch(14, [3, 5], dim=128, part_dim=64, null_count=0, bias=False)
+    st = b.conv_states.copy()
+    res = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, None, st,
+                               b.cache_indices, b.has_initial_state, b.query_start_loc,
+                               b.null_block_id, 0, want_preact=True, lib=lib)
+    _check_against_columns(b, res, st, exact=True)
+
+
+def pin_float64_windows(lib) -> None:
+    """Window dot products in float64 (all lengths around the 3-row history and
+    64-row chunk edges) within four fp32 roundings."""
+    lengths = [1, 2, 3, 4, 5, 63, 64, 65, 129]
+    b = small_batch(21, lengths, dim=192, part_dim=64, null_count=2, row_stride=232,
+                    cache_lines=16)
+    st = b.conv_states.copy()
+    res = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
+                               b.cache_indices, b.has_initial_state, b.query_start_loc,
+                               b.null_block_id, b.activation, want_preact=True, lib=lib)
+    _check_against_columns(b, res, st, exact=False)
+
+
+def pin_torch_conv1d(lib, b: workloads.Batch | None = None) -> None:
+    """torch.nn.functional.conv1d(groups=dim) in float64 over [history ; x_seq]^T,
+    per sequence, against the oracle's pre-activation (library special case)."""
+    if b is None:
+        b = small_batch(31, [40, 1, 2, 77, 3, 130], dim=256, part_dim=128, null_count=1,
+                        row_stride=320, col_offset=64, cache_lines=9)
+    st = b.conv_states.copy()
+    res = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
+                               b.cache_indices, b.has_initial_state, b.query_start_loc,
+                               b.null_block_id, b.activation, want_preact=True, lib=lib)
+    pre = plane_view(res["preact"], b).astype(np.float64)
+    w = torch.from_numpy(b.weight.astype(np.float64)).unsqueeze(1)  # (dim, 1, 4)
+    bias_t = None if b.bias is None else torch.from_numpy(b.bias.astype(np.float64))
+    for s in range(b.num_seqs):
+        a, e = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+        if e <= a:
+            continue
+        line = int(b.cache_indices[s])
+        hist = np.zeros((3, b.dim))
+        if line != b.null_block_id and b.has_initial_state[s]:
+            hist = b.conv_states[line].T.astype(np.float64)
+        xs = torch_bf16_to_f32(b.x_buf[a:e, b.col_offset:b.col_offset + b.dim]).astype(np.float64)
+        inp = torch.from_numpy(np.concatenate([hist, xs]).T.copy()).unsqueeze(0)  # (1, dim, L+3)
+        ref = torch.nn.functional.conv1d(inp, w, bias_t, groups=b.dim)[0].T.numpy()  # (L, dim)
+        mag = torch.nn.functional.conv1d(inp.abs(), w.abs(), None if bias_t is None
+                                         else bias_t.abs(), groups=b.dim)[0].T.numpy()
+        err = np.abs(pre[a:e] - ref)
+        assert (err <= 4 * U * mag + 1e-40).all(), (s, float(err.max()))
+
+
+def pin_silu_and_rounding(lib) -> None:
+    """SiLU against torch's float64 silu within a few fp32 ulp, and the stored
+    bf16 against torch's RNE of the activated value."""
+    b = small_batch(41, [50, 3, 90], dim=128, part_dim=64, null_count=0, cache_lines=5,
+                    x_std=3.0, w_range=1.0)
+    st = b.conv_states.copy()
+    res = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
+                               b.cache_indices, b.has_initial_state, b.query_start_loc,
+                               b.null_block_id, 1, want_preact=True, want_act=True, lib=lib)
+    live = ~np.isnan(res["preact"])
+    pre = res["preact"][live].astype(np.float64)
+    act = res["act"][live].astype(np.float64)
+    ref = torch.nn.functional.silu(torch.from_numpy(pre)).numpy()
+    assert (np.abs(act - ref) <= 8 * U * np.abs(ref) + 1e-44).all()
+    assert np.array_equal(res["out"][live], torch_f32_to_bf16(res["act"][live]))
+    # Values at the extremes of the SiLU, against float64 (denormal-free range).
+    a = np.array([-80.0, -20.0, -3.5, -1e-3, 0.0, 1e-30, 0.5, 7.25, 30.0, 1e30], dtype=np.float32)
+    got = oracle.silu(a, lib).astype(np.float64)
+    ref = torch.nn.functional.silu(torch.from_numpy(a.astype(np.float64))).numpy()
+    assert (np.abs(got - ref) <= 8 * U * np.abs(ref) + 1e-44).all()
+
+
+def pin_closed_forms(lib) -> None:
+    """Identity (w = e3), shift (w = e0) and bias-only (w = 0) kernels."""
+    base = small_batch(51, [1, 2, 5, 40], dim=128, part_dim=64, null_count=1, his_p=1.0,
+                       activation=0, bias=False, cache_lines=8)
+    xv = base.x_buf[:, base.col_offset:base.col_offset + base.dim]
+    qsl = base.query_start_loc
+
+    # identity: out = x exactly (a -0 input gives +0, since the chain starts at +0)
+    b = base.copy()
+    b.weight[:] = 0
+    b.weight[:, 3] = 1
+    out = plane_view(run_oracle(b, lib)["out"], b)
+    want = np.where((xv == 0x8000), 0, xv)
+    assert np.array_equal(out[qsl[0]:qsl[-1]], want[qsl[0]:qsl[-1]])
+
+    # shift by three rows: out[t] = x[t-3], or the rounded history for t < 3
+    b = base.copy()
+    b.weight[:] = 0
+    b.weight[:, 0] = 1
+    out = plane_view(run_oracle(b, lib)["out"], b)
+    for s in range(b.num_seqs):
+        a, e = int(qsl[s]), int(qsl[s + 1])
+        line = int(b.cache_indices[s])
+        hist = np.zeros((3, b.dim), dtype=np.float32)
+        if line != b.null_block_id and b.has_initial_state[s]:
+            hist = base.conv_states[line].T.copy()
+        for t in range(e - a):
+            want_row = xv[a + t - 3] if t >= 3 else torch_f32_to_bf16(hist[t] + np.float32(0))
+            want_row = np.where(want_row == 0x8000, 0, want_row)
+            assert np.array_equal(out[a + t], want_row), (s, t)
+
+    # bias only: out = bf16(bias) on every sequence row
+    b = base.copy()
+    b.weight[:] = 0
+    b.bias = np.linspace(-3, 3, b.dim).astype(np.float32)
+    out = plane_view(run_oracle(b, lib)["out"], b)
+    want = torch_f32_to_bf16(b.bias)
+    for t in range(int(qsl[0]), int(qsl[-1])):
+        assert np.array_equal(out[t], want)
+
+
+def _sub_batch(b: workloads.Batch, ranges, his, states) -> workloads.Batch:
+    """A batch holding, for each sequence, rows [lo, hi) of the original x."""
+    rows = np.concatenate([np.arange(lo, hi) for lo, hi in ranges]).astype(np.int64)
+    lens = [hi - lo for lo, hi in ranges]
+    qsl = np.zeros(len(lens) + 1, dtype=np.int32)
+    qsl[1:] = np.cumsum(lens)
+    c = b.copy()
+    c.x_buf = np.ascontiguousarray(b.x_buf[rows])
+    c.query_start_loc = qsl
+    c.has_initial_state = np.asarray(his, dtype=np.uint8)
+    c.conv_states = states
+    return c
+
+
+def pin_chunk_carry(lib) -> None:
+    """Splitting every sequence in two calls with the state carried equals one call."""
+    lengths = [70, 5, 129, 4, 66]
+    base = small_batch(61, lengths, dim=64, part_dim=64, null_count=0, his_p=0.5,
+                       cache_lines=8)
+    one = base.copy()
+    full = run_oracle(one, lib)
+    full_out = plane_view(full["out"], base)
+    qsl = base.query_start_loc
+    for m in [1, 2, 3, 17, 64, None]:
+        first, second = [], []
+        for s in range(base.num_seqs):
+            a, e = int(qsl[s]), int(qsl[s + 1])
+            cut = (e - a - 1) if m is None else min(m, e - a - 1)
+            first.append((a, a + cut))
+            second.append((a + cut, e))
+        c1 = _sub_batch(base, first, base.has_initial_state, base.conv_states.copy())
+        o1 = plane_view(run_oracle(c1, lib)["out"], c1)
+        c2 = _sub_batch(base, second, np.ones(base.num_seqs), c1.conv_states)
+        o2 = plane_view(run_oracle(c2, lib)["out"], c2)
+        r1 = r2 = 0
+        for s in range(base.num_seqs):
+            (a1, b1), (a2, b2) = first[s], second[s]
+            assert np.array_equal(o1[r1:r1 + b1 - a1], full_out[a1:b1]), (m, s)
+            assert np.array_equal(o2[r2:r2 + b2 - a2], full_out[a2:b2]), (m, s)
+            r1 += b1 - a1
+            r2 += b2 - a2
+        assert np.array_equal(c2.conv_states.view(np.uint32), one.conv_states.view(np.uint32)), m
+
+
+def pin_zero_history(lib) -> None:
+    """has_initial_state = 0 behaves as a zero state line with has_initial_state = 1,
+    and a null-block sequence computes with zero history."""
+    b = small_batch(71, [5, 2, 30], dim=128, part_dim=64, null_count=0, his_p=0.0,
+                    cache_lines=6)
+    r0 = run_oracle(b.copy(), lib)
+    z = b.copy()
+    z.has_initial_state[:] = 1
+    for line in z.cache_indices:
+        z.conv_states[line] = 0
+    r1 = run_oracle(z, lib)
+    assert np.array_equal(r0["out"], r1["out"])
+    n = b.copy()
+    n.cache_indices[:] = n.null_block_id
+    n.has_initial_state[:] = 1
+    r2 = run_oracle(n, lib)
+    assert np.array_equal(r0["out"], r2["out"])
+
+
+def pin_short_state_shift(lib) -> None:
+    """Sequences shorter than 3 tokens shift the state: new = [old[L:], x rows]."""
+    for his in (1, 0):
+        b = small_batch(81 + his, [1, 2, 3], dim=64, part_dim=64, null_count=0,
+                        his_p=float(his), cache_lines=5)
+        st = b.conv_states.copy()
+        run = b.copy()
+        run.conv_states = st
+        run_oracle(run, lib)
+        for s, L in enumerate([1, 2, 3]):
+            a = int(b.query_start_loc[s])
+            line = int(b.cache_indices[s])
+            old = b.conv_states[line] if his else np.zeros((b.dim, 3), dtype=np.float32)
+            xs = torch_bf16_to_f32(b.x_buf[a:a + L, b.col_offset:b.col_offset + b.dim]).T
+            want = np.concatenate([old[:, L:], xs], axis=1)
+            assert np.array_equal(st[line].view(np.uint32), want.view(np.uint32)), (his, L)
+
+
+def pin_permutation(lib) -> None:
+    """Permuting the sequences permutes the outputs and leaves the states equal."""
+    lengths = [9, 1, 33, 4, 17]
+    b = small_batch(91, lengths, dim=128, part_dim=64, null_count=1, cache_lines=8)
+    r = run_oracle(b.copy(), lib)
+    perm = [3, 0, 4, 2, 1]
+    qsl = b.query_start_loc
+    ranges = [(int(qsl[s]), int(qsl[s + 1])) for s in perm]
+    p = _sub_batch(b, ranges, b.has_initial_state[perm], b.conv_states.copy())
+    p.cache_indices = b.cache_indices[perm].copy()
+    rp = run_oracle(p, lib)
+    want_states = b.copy()
+    run_oracle(want_states, lib)
+    assert np.array_equal(p.conv_states.view(np.uint32), want_states.conv_states.view(np.uint32))
+    out, outp = plane_view(r["out"], b), plane_view(rp["out"], p)
+    row = 0
+    for lo, hi in ranges:
+        assert np.array_equal(outp[row:row + hi - lo], out[lo:hi])
+        row += hi - lo
+
+
+def pin_untouched(lib) -> None:
+    """Lines not referenced, the null block's sequence, rows outside
+    [qsl[0], qsl[N]) and empty calls leave memory as it was."""
+    b = small_batch(101, [4, 0, 9, 2], dim=128, part_dim=64, null_count=1, cache_lines=10,
+                    tokens=30, first_token=5)
+    st = b.conv_states.copy()
+    run = b.copy()
+    run.conv_states = st
+    out = run_oracle(run, lib)["out"]
+    rows = plane_view(out, b)
+    assert (rows[:5] == 0xFFFF).all() and (rows[5 + 15:] == 0xFFFF).all()
+    live = {int(c) for c, L in zip(b.cache_indices, np.diff(b.query_start_loc))
+            if c != b.null_block_id and L > 0}
+    for line in range(b.cache_lines):
+        if line not in live:
+            assert np.array_equal(st[line].view(np.uint32), b.conv_states[line].view(np.uint32))
+    # empty calls
+    for qsl in (np.array([0], dtype=np.int32), np.array([0, 0, 0], dtype=np.int32)):
+        e = b.copy()
+        e.query_start_loc = qsl
+        e.cache_indices = b.cache_indices[:qsl.size - 1].copy()
+        e.has_initial_state = b.has_initial_state[:qsl.size - 1].copy()
+        o = run_oracle(e, lib)["out"]
+        assert (o == 0xFFFF).all()
+        assert np.array_equal(e.conv_states.view(np.uint32), b.conv_states.view(np.uint32))
+
+
+def pin_metadata_checks(lib) -> None:
+    """Malformed metadata is rejected."""
+    good = (np.array([0, 1], dtype=np.int32), np.array([0, 2, 5], dtype=np.int32))
+    assert oracle.check_metadata(8, 4, *good, -1, lib=lib)[0] == oracle.REF_OK
+    cases = [
+        (np.array([0, 1]), np.array([0, 6, 5]), oracle.REF_BAD_QSL),  # decreasing
+        (np.array([0, 1]), np.array([-1, 2, 5]), oracle.REF_BAD_QSL),  # negative start
+        (np.array([0, 1]), np.array([0, 2, 9]), oracle.REF_BAD_QSL),  # past tokens
+        (np.array([0, 4]), np.array([0, 2, 5]), oracle.REF_BAD_CACHE_INDEX),
+        (np.array([-2, 1]), np.array([0, 2, 5]), oracle.REF_BAD_CACHE_INDEX),
+        (np.array([1, 1]), np.array([0, 2, 5]), oracle.REF_DUP_CACHE_INDEX),
+    ]
+    for ci, qsl, rc in cases:
+        assert oracle.check_metadata(8, 4, ci, qsl, -1, lib=lib)[0] == rc
+    # two null-block sequences are not a duplicate
+    assert oracle.check_metadata(8, 4, np.array([-1, -1]), good[1], -1, lib=lib)[0] == 0
+
+
+ALL_PINS = [
+    pin_bf16_widen, pin_bf16_rne, pin_exact_rational, pin_float64_windows, pin_torch_conv1d,
+    pin_silu_and_rounding, pin_closed_forms, pin_chunk_carry, pin_zero_history,
+    pin_short_state_shift, pin_permutation, pin_untouched, pin_metadata_checks,
+]

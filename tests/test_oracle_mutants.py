@@ -1,0 +1,64 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU,
+in a temporary directory), builds it and runs the pins against it: at least
+one pin has to fail.  The real oracle is never modified.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "kda_conv_ref.c")
+
+# (name, text in the oracle, replacement).  Each text occurs exactly once.
+MUTANTS = [
+    ("taps_reversed", "acc = fmaf(v, weight[c * 4 + j], acc);",
+     "acc = fmaf(v, weight[c * 4 + (3 - j)], acc);"),
+    ("tap_dropped", "for (int j = 0; j < 4; ++j) {", "for (int j = 1; j < 4; ++j) {"),
+    ("mul_then_add", "acc = fmaf(v, weight[c * 4 + j], acc);",
+     "acc = v * weight[c * 4 + j] + acc;"),
+    ("bias_dropped", "float acc = bias ? bias[c] : 0.0f;", "float acc = 0.0f;"),
+    ("state_read_reversed", "h[k] = conv_states[(line * dim + c) * 3 + k];",
+     "h[k] = conv_states[(line * dim + c) * 3 + (2 - k)];"),
+    ("state_write_reversed", "conv_states[(line * dim + c) * 3 + k] = ns[k];",
+     "conv_states[(line * dim + c) * 3 + k] = ns[2 - k];"),
+    ("state_rows_off_by_one", "int64_t r = len - 3 + k;", "int64_t r = len - 4 + k;"),
+    ("his_ignored", "int read_state = !is_null && has_initial_state[s];",
+     "int read_state = !is_null;"),
+    ("null_rejected", "if (line == null_block_id) continue;", ""),
+    ("round_truncates", "if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) {", "if (0) {"),
+    ("ties_away", "if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) {",
+     "if (lo >= 0x8000u) {"),
+    ("silu_sign", "float e = expf(-a);", "float e = expf(a);"),
+    ("planes_row_major", "int64_t o = (plane * tokens + (a + t)) * part_dim + col;",
+     "int64_t o = (a + t) * dim + c;"),
+    ("widen_shift", "return f32_from_bits((uint32_t)h << 16);",
+     "return f32_from_bits(((uint32_t)h << 16) | 1u);"),
+]
+
+
+def test_real_oracle_has_every_mutation_site():
+    text = open(SRC).read()
+    for name, old, _ in MUTANTS:
+        assert text.count(old) == 1, name
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    text = open(SRC).read()
+    assert text.count(old) == 1
+    src = tmp_path / f"mutant_{name}.c"
+    src.write_text(text.replace(old, new))
+    lib = oracle.load(oracle.build(force=True, src=str(src), out=str(tmp_path / f"{name}.so")))
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError) as e:  # ValueError: the mutant rejected a call
+            caught.append((pin.__name__, type(e).__name__))
+            break
+    assert caught, f"no pin caught mutant {name}"

@@ -1,0 +1,185 @@
+"""Seeded synthetic inputs for the packed varlen causal conv1d.
+
+This module only draws random numbers and lays them out; it holds none of
+the conv's arithmetic.  The same host arrays feed the CPU oracle and (copied
+to the device) the CUDA library, so both sides see identical bytes.
+
+Every draw comes from a CPU ``torch.Generator`` seeded per workload, in the
+order written in ``make_batch``.  bf16 inputs are fp32 normal samples
+converted by torch's own ``.to(torch.bfloat16)``.
+
+Workloads (shapes from the Kimi-K3 KDA in_proj as the vLLM page
+"vllm.models.kimi_k3.nvidia.ops.kda_conv" sizes it: 3 x 1536 channels, 16K
+token prefill chunks, row-strided bf16 slices of a wider projection):
+
+  tiny          1 x 64 tokens, dim 384 = 3 x 128, dense rows, SiLU, seed 0
+  varlen        8 sequences, lengths U[1,512], dim 4608 = 3 x 1536, row stride
+                6400, one padding sequence (null block), his ~ Bernoulli(0.5),
+                SiLU, seed 1
+  long16k       1 x 16384 tokens, dim 4608, row stride 6400, SiLU, seed 2
+  short_decode  256 sequences with lengths U[1,128] followed by 1024 one-token
+                (decode-shaped) sequences in one call, dim 4608, row stride
+                6400, 2048 cache lines, his ~ Bernoulli(0.8), SiLU, seed 3
+  large_nobias  4 x 8192 tokens, dim 3264 = 3 x 1088, dense rows, x ~ N(0, 2^2),
+                weight U(-1, 1), no bias, no activation, seed 4
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+NULL_BLOCK_ID = -1  # the pages do not print the constant; -1 is no valid cache line
+
+
+@dataclass
+class Batch:
+    """One call's inputs, as host numpy arrays."""
+
+    name: str
+    x_buf: np.ndarray  # (tokens, row_stride) uint16: bf16 bits of the whole in_proj rows
+    col_offset: int  # x = x_buf[:, col_offset:col_offset + dim]
+    dim: int
+    part_dim: int
+    weight: np.ndarray  # (dim, 4) float32
+    bias: np.ndarray | None  # (dim,) float32
+    conv_states: np.ndarray  # (cache_lines, dim, 3) float32
+    cache_indices: np.ndarray  # (num_seqs,) int32
+    has_initial_state: np.ndarray  # (num_seqs,) uint8 (0/1)
+    query_start_loc: np.ndarray  # (num_seqs + 1,) int32
+    null_block_id: int
+    activation: int  # 0 none, 1 SiLU
+    seed: int
+    notes: dict = field(default_factory=dict)
+
+    @property
+    def tokens(self) -> int:
+        return int(self.x_buf.shape[0])
+
+    @property
+    def row_stride(self) -> int:
+        return int(self.x_buf.shape[1])
+
+    @property
+    def num_seqs(self) -> int:
+        return int(self.query_start_loc.size - 1)
+
+    @property
+    def cache_lines(self) -> int:
+        return int(self.conv_states.shape[0])
+
+    def copy(self) -> "Batch":
+        """Deep copy (conv_states is updated in place by a call)."""
+        return Batch(
+            self.name, self.x_buf.copy(), self.col_offset, self.dim, self.part_dim,
+            self.weight.copy(), None if self.bias is None else self.bias.copy(),
+            self.conv_states.copy(), self.cache_indices.copy(), self.has_initial_state.copy(),
+            self.query_start_loc.copy(), self.null_block_id, self.activation, self.seed,
+            dict(self.notes))
+
+
+def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def make_batch(name: str, seed: int, lengths, dim: int, part_dim: int, row_stride: int,
+               cache_lines: int, *, col_offset: int = 0, x_std: float = 1.0,
+               w_range: float = 0.5, bias_std: float | None = 0.1, activation: int = 1,
+               his_p: float = 1.0, his: list[int] | None = None, null_count: int = 0,
+               tokens: int | None = None, first_token: int = 0) -> Batch:
+    """Draws one batch.
+
+    Draw order: lengths are given; x (tokens, row_stride) ~ N(0, x_std^2);
+    weight (dim, 4) ~ U(-w_range, w_range); bias (dim) ~ N(0, bias_std^2) if
+    bias_std is not None; conv_states (cache_lines, dim, 3) ~ N(0, 1);
+    cache_indices = the first num_seqs of a random permutation of the cache
+    lines; has_initial_state ~ Bernoulli(his_p) unless given; then
+    `null_count` distinct random sequences get NULL_BLOCK_ID as cache index.
+
+    Sequences are packed back to back from `first_token`; `tokens` (default:
+    the end of the last sequence) may leave rows after the last sequence that
+    no sequence owns.
+    """
+    g = torch.Generator().manual_seed(seed)
+    lengths = [int(v) for v in lengths]
+    n = len(lengths)
+    qsl = np.zeros(n + 1, dtype=np.int32)
+    qsl[0] = first_token
+    qsl[1:] = first_token + np.cumsum(np.asarray(lengths, dtype=np.int64))
+    total = int(qsl[-1]) if tokens is None else int(tokens)
+    assert total >= int(qsl[-1])
+    x = _bf16_bits(torch.randn(total, row_stride, generator=g) * x_std)
+    w = ((torch.rand(dim, 4, generator=g) * 2.0 - 1.0) * w_range).numpy().astype(np.float32)
+    b = None
+    if bias_std is not None:
+        b = (torch.randn(dim, generator=g) * bias_std).numpy().astype(np.float32)
+    s = torch.randn(cache_lines, dim, 3, generator=g).numpy().astype(np.float32)
+    assert n <= cache_lines
+    ci = torch.randperm(cache_lines, generator=g)[:n].numpy().astype(np.int32)
+    if his is None:
+        hv = (torch.rand(n, generator=g) < his_p).numpy().astype(np.uint8)
+    else:
+        hv = np.asarray(his, dtype=np.uint8)
+    if null_count:
+        pos = torch.randperm(n, generator=g)[:null_count].numpy()
+        ci[pos] = NULL_BLOCK_ID
+    return Batch(name, np.ascontiguousarray(x), col_offset, dim, part_dim, np.ascontiguousarray(w),
+                 b, np.ascontiguousarray(s), ci, hv, qsl, NULL_BLOCK_ID, activation, seed)
+
+
+def _lengths(seed: int, n: int, lo: int, hi: int) -> list[int]:
+    g = torch.Generator().manual_seed(seed + 1000)
+    return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
+
+
+def tiny() -> Batch:
+    # cache_indices = [2] as the workload fixes it, regardless of the permutation draw.
+    b = make_batch("tiny", 0, [64], 384, 128, 384, 4, his=[1])
+    b.cache_indices[:] = 2
+    return b
+
+
+def varlen() -> Batch:
+    return make_batch("varlen", 1, _lengths(1, 8, 1, 512), 4608, 1536, 6400, 64,
+                      his_p=0.5, null_count=1)
+
+
+def long16k() -> Batch:
+    return make_batch("long16k", 2, [16384], 4608, 1536, 6400, 8, his=[1])
+
+
+def short_decode() -> Batch:
+    lens = _lengths(3, 256, 1, 128) + [1] * 1024
+    return make_batch("short_decode", 3, lens, 4608, 1536, 6400, 2048, his_p=0.8)
+
+
+def large_nobias() -> Batch:
+    return make_batch("large_nobias", 4, [8192] * 4, 3264, 1088, 3264, 16, x_std=2.0,
+                      w_range=1.0, bias_std=None, activation=0, his=[1, 0, 1, 0])
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "varlen": varlen,
+    "long16k": long16k,
+    "short_decode": short_decode,
+    "large_nobias": large_nobias,
+}
+
+
+def algorithmic_bytes(b: Batch) -> int:
+    """Bytes a call must move at minimum: x read once, out written once, each
+    referenced state line read (if it has an initial state) and written, the
+    weight and bias read once.  Halo re-reads are not counted."""
+    qsl = b.query_start_loc.astype(np.int64)
+    lens = qsl[1:] - qsl[:-1]
+    live = lens > 0
+    not_null = b.cache_indices != b.null_block_id
+    rows = int(lens[live].sum())
+    reads = int(np.count_nonzero(live & not_null & (b.has_initial_state != 0)))
+    writes = int(np.count_nonzero(live & not_null))
+    d = b.dim
+    return (2 * rows * d + 2 * rows * d + 12 * d * reads + 12 * d * writes + 16 * d
+            + (4 * d if b.bias is not None else 0))
