@@ -1,0 +1,431 @@
+"""Benchmark: HBM GB/s of the packed varlen causal conv1d on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload long16k]
+                    [--impl ours|reference]
+
+One step = one kda_packed_conv1d call over one batch of the workload (the
+whole hot path: program map, state read/write, taps, SiLU, rounding, plane
+stores).  The default workload is one 16384-token prefill chunk of the
+Kimi-K3 KDA Q|K|V projection: dim 4608 = 3 x 1536, bf16 x with row stride
+6400, FP32 weights / bias / conv state, SiLU.
+
+value = algorithmic bytes moved by all ranks / timed region (GB/s).  The
+algorithmic bytes are x read once + out written once + state lines read and
+written + weight and bias (halo re-reads not counted).  Consecutive steps use
+different copies of the inputs and outputs (rotating sets whose total is far
+above the 129 MB L2), so no step finds its data in L2.
+
+--impl reference times the CPU oracle (plain single-threaded C) on a bounded
+sample of the same workload on the host cores, as the reference arm.
+
+Prints one JSON line (rank 0).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "HBM GB/s (read+write) & % of GB300 peak; packed QKV conv 16K x 3x1536 bf16"
+UNIT = "GB/s"
+PAGE_GBS = 4800.0  # the page's ~4.8 TB/s for its packed kernel at 2K-16K x 3x1536 on GB300
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "linear_attention_prefill_varlen_gb300", "csrc", "kda_conv.cu")
+PROFILE = os.path.join(ROOT, "profiles", "kda_packed_conv1d_long16k.md")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="long16k", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic() -> int | None:
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source (its sha line matches)."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not sha or not tr or sha.group(1) != kernel_sha():
+        return None
+    return int(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{device_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict | None:
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        sm_max = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[0] >= 0.5 * sm_max] or rows
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(1, 5) if r[2][i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": sm_max,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+class Dist:
+    """Barrier and max-over-ranks for N > 1 (one process per GPU)."""
+
+    def __init__(self, world: int, backend: str):
+        self.world = world
+        self.pg = None
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float, device) -> float:
+        if self.pg is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
+    """Device copies of one batch.  dense_x stores x as (tokens, dim) contiguous."""
+    x_np = b.x_buf[:, b.col_offset:b.col_offset + b.dim] if dense_x else b.x_buf
+    x = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).to(dev)
+    return {
+        "x": x,
+        "x_ptr": x.data_ptr() + (0 if dense_x else 2 * b.col_offset),
+        "x_row_stride": b.dim if dense_x else b.row_stride,
+        "weight": torch.from_numpy(b.weight).to(dev),
+        "bias": None if b.bias is None else torch.from_numpy(b.bias).to(dev),
+        "conv_states": torch.from_numpy(b.conv_states).to(dev),
+        "cache_indices": torch.from_numpy(b.cache_indices).to(dev),
+        "has_initial_state": torch.from_numpy(b.has_initial_state).to(dev),
+        "query_start_loc": torch.from_numpy(b.query_start_loc).to(dev),
+        "out": torch.empty((b.dim // b.part_dim, b.tokens, b.part_dim), dtype=torch.int16,
+                           device=dev),
+    }
+
+
+def call(pkg, b: workloads.Batch, s: dict, stream) -> None:
+    pkg.kda_packed_conv1d(s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim,
+                          s["weight"], s["bias"], s["conv_states"], s["cache_indices"],
+                          s["has_initial_state"], s["query_start_loc"], b.num_seqs,
+                          b.null_block_id, b.activation, s["out"], stream)
+
+
+def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, dist: Dist,
+                dev) -> dict:
+    """W untimed steps, then exactly K timed steps between barrier+sync pairs.
+    Each step uses the next input/output set; every launch is bracketed by
+    events on the launching stream."""
+    stream = torch.cuda.Stream(device=dev)
+    for i in range(warmup):
+        call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index or 0) as clocks:
+        region0.record(stream)
+        for i in range(steps):
+            starts[i].record(stream)
+            call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+            ends[i].record(stream)
+        region1.record(stream)
+        torch.cuda.synchronize(dev)
+    dist.barrier()
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return {"region_ms": region0.elapsed_time(region1), "kernel_ms": kernel_ms,
+            "clocks": clocks.summary()}
+
+
+def time_e2e(pkg, b: workloads.Batch, steps: int, dev) -> dict:
+    """The same call with HOST inputs and result: each step copies x (the
+    (tokens, dim) slice) and the metadata from pinned host memory, runs the
+    conv, and copies the output planes back to pinned host memory."""
+    x_host = torch.from_numpy(np.ascontiguousarray(
+        b.x_buf[:, b.col_offset:b.col_offset + b.dim]).view(np.int16)).pin_memory()
+    meta_host = [torch.from_numpy(a).pin_memory() for a in
+                 (b.query_start_loc, b.cache_indices, b.has_initial_state)]
+    s = upload(b, dev, dense_x=True)
+    out_host = torch.empty(s["out"].shape, dtype=torch.int16).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    meta_dev = [s["query_start_loc"], s["cache_indices"], s["has_initial_state"]]
+
+    def step():
+        with torch.cuda.stream(stream):
+            s["x"].copy_(x_host, non_blocking=True)
+            for d, h in zip(meta_dev, meta_host):
+                d.copy_(h, non_blocking=True)
+            call(pkg, b, s, stream.cuda_stream)
+            out_host.copy_(s["out"], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    h2d = x_host.numel() * 2 + sum(h.numel() * h.element_size() for h in meta_host)
+    d2h = out_host.numel() * 2
+    return {"ms": ms, "h2d": h2d, "d2h": d2h}
+
+
+def oracle_sample(b: workloads.Batch, seconds: float, max_reps: int = 50) -> dict:
+    """The CPU oracle, as it stands, on the whole workload batch, repeated
+    until about `seconds` of work (single thread)."""
+    import oracle
+
+    oracle.load()
+    reps, t_total = 0, 0.0
+    while reps < max_reps and (reps == 0 or t_total < seconds):
+        st = b.conv_states.copy()
+        t = time.perf_counter()
+        oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
+                             b.cache_indices, b.has_initial_state, b.query_start_loc,
+                             b.null_block_id, b.activation)
+        t_total += time.perf_counter() - t
+        reps += 1
+    nbytes = workloads.algorithmic_bytes(b)
+    return {"value": nbytes * reps / t_total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x the whole {b.name} batch ({b.tokens} tokens x {b.dim} "
+                      f"channels), single-threaded C, {t_total:.1f} s"}
+
+
+def sample_rows(b: workloads.Batch, rows: int) -> workloads.Batch:
+    """The first `rows` token rows of a batch as its own call (sequences cut there)."""
+    c = b.copy()
+    c.x_buf = np.ascontiguousarray(b.x_buf[:rows])
+    qsl = np.minimum(b.query_start_loc, rows).astype(np.int32)
+    c.query_start_loc = qsl
+    return c
+
+
+def base_line(args, world: int, value: float, ms: float, b: workloads.Batch, extra: dict) -> dict:
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": b.name, "tokens": b.tokens, "num_seqs": b.num_seqs, "dim": b.dim,
+            "part_dim": b.part_dim, "x_row_stride": b.row_stride,
+            "activation": "silu" if b.activation else "none", "bias": b.bias is not None,
+            "storage": "x/out bf16, weight/bias/conv_state fp32",
+            "bytes_per_step_per_gpu": workloads.algorithmic_bytes(b),
+            "parallelism": f"replicas x{world}",
+        },
+    }
+    line.update(extra)
+    return line
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return  # the reference arm runs on rank 0 alone
+    import oracle
+
+    oracle.load()
+    b = workloads.WORKLOADS[args.workload]()
+    probe = sample_rows(b, min(b.tokens, 256))
+    t = time.perf_counter()
+    oracle_sample(probe, 0.0, max_reps=1)
+    per_row = (time.perf_counter() - t) / probe.tokens
+    budget = 45.0 / max(1, args.steps + args.warmup)
+    rows = int(max(16, min(b.tokens, budget / max(per_row, 1e-9))))
+    s = sample_rows(b, rows)
+    for _ in range(args.warmup):
+        oracle_sample(s, 0.0, max_reps=1)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(s, 0.0, max_reps=1)
+    secs = time.perf_counter() - t
+    nbytes = workloads.algorithmic_bytes(s)
+    value = nbytes * args.steps / secs / 1e9
+    sample = (f"per step: the first {rows} token rows of the {b.name} batch (all {b.dim} "
+              f"channels), single-threaded C oracle")
+    line = base_line(args, world, value, secs * 1e3 / args.steps, b, {
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    })
+    line["config"]["bytes_per_step_per_gpu"] = nbytes
+    line["config"]["sample_rows"] = rows
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args) -> None:
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = Dist(world, "nccl")
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    pkg.lib()
+    b = workloads.WORKLOADS[args.workload]()
+    nbytes = workloads.algorithmic_bytes(b)
+    footprint = b.x_buf.nbytes + 2 * b.tokens * b.dim
+    n_sets = max(3, -(-4 * L2_BYTES // footprint))
+    sets = [upload(b, dev) for _ in range(n_sets)]
+    torch.cuda.synchronize(dev)
+
+    t = time_device(pkg, b, sets, args.steps, args.warmup, dist, dev)
+    region_ms = dist.max(t["region_ms"], dev)
+    kern_mean = statistics.fmean(t["kernel_ms"])
+    kern_mean_max = dist.max(kern_mean, dev)
+    ms_per_step = region_ms / args.steps
+    value = world * nbytes / (ms_per_step * 1e-3) / 1e9
+
+    e2e = time_e2e(pkg, b, args.e2e_steps, dev)
+    e2e_ms = dist.max(e2e["ms"], dev)
+    del sets
+    dist.close()
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / (kern_mean_max * 1e-3) / 1e9
+    extra = {
+        "vs_baseline": round(value / world / PAGE_GBS, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(), "peak_source": peak_kind,
+                     "kernel": "kda_packed_conv1d_kernel",
+                     "kernel_us_mean": round(kern_mean_max * 1e3, 3),
+                     "kernel_us_median": round(statistics.median(t["kernel_ms"]) * 1e3, 3)},
+        "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": round(e2e_ms, 4),
+                "note": "x staged dense (row stride = dim) from pinned host memory"},
+        "gpu_launches": args.steps,
+        "clocks": t["clocks"],
+        "tokens_per_s": round(world * b.tokens / (ms_per_step * 1e-3), 1),
+    }
+    line = base_line(args, world, value, ms_per_step, b, extra)
+    line["config"]["l2"] = (f"{n_sets} rotating input/output sets of {footprint / 1e6:.0f} MB "
+                            f"(> 129 MB L2); no step reuses the previous step's buffers")
+    line["config"]["kernel_source_sha"] = kernel_sha()
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(b, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,176 @@
+/*
+ * kda_conv.h -- C ABI of the GB300 (sm_103a) packed varlen causal depthwise
+ * conv1d that the Kimi-K3 KDA layer runs over the Q|K|V columns of its
+ * in_proj output before the delta-rule recurrence.
+ *
+ * The operation is the one the vLLM page "vllm.models.kimi_k3.nvidia.ops.
+ * kda_conv" (docs.vllm.ai) describes:
+ *   - module docstring, 3rd paragraph: bf16 Q|K|V columns are read in place,
+ *     widened exactly to FP32, convolved with FP32 weights and an FP32 conv
+ *     state, passed through SiLU, rounded to bf16 to nearest even and stored
+ *     as dense (tokens, part_dim) planes of one buffer;
+ *   - module docstring, 4th paragraph: programs find their (sequence, token
+ *     chunk) on the device from query_start_loc, so a launch needs no host
+ *     table and can be captured in a CUDA graph; only a sequence's first
+ *     chunk reads its conv state and that same program writes the update;
+ *   - packed_causal_conv1d_fn and its docstring: the argument set (x, weight,
+ *     bias, conv_states, query_start_loc, cache_indices, has_initial_state,
+ *     part_dim, activation, null_block_id), width-4 taps, conv_states
+ *     (cache lines, dim, 3) updated in place, result (dim/part_dim, tokens,
+ *     part_dim), and the early return when there are no tokens or sequences;
+ *   - packed_causal_conv1d_supported: what inputs the method accepts
+ *     (unit channel stride, FP32 weight (dim, 4) and state, part_dim a
+ *     multiple of 64 that divides dim).
+ *
+ * For token t of sequence s (rows query_start_loc[s] .. query_start_loc[s+1]-1)
+ * and channel c, with v(j) the FP32 value of input row t-3+j (history rows
+ * -3, -2, -1 come from the conv state, index 0 oldest):
+ *     acc = bias ? bias[c] : +0.0f
+ *     acc = fmaf(v(j), weight[c][j], acc)      for j = 0, 1, 2, 3 in that order
+ *     y   = activation == SiLU ? acc / (1 + exp(-acc)) : acc
+ *     out[c / part_dim][t][c % part_dim] = bf16_round_nearest_even(y)
+ * and afterwards conv_states[cache_indices[s]][c][k] = v of row L-3+k
+ * (k = 0, 1, 2; L = the sequence length), i.e. the last three rows of
+ * [history ; the sequence's input rows].
+ *
+ * All entry points are synchronous with respect to the host only where
+ * stated; the conv calls are asynchronous on the given stream, allocate
+ * nothing, never synchronise, and launch a grid that depends only on the
+ * scalar arguments (so a captured launch replays correctly for new metadata
+ * values of the same tokens / num_seqs).
+ */
+#ifndef KDA_CONV_H_
+#define KDA_CONV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (cudaStream_t / CUstream); NULL is the legacy default stream. */
+typedef void *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* NULL required pointer, negative size, bad activation, ... */
+    KDA_ERR_UNSUPPORTED = 2, /* shape the method does not cover (part_dim % 64, dim % part_dim) */
+    KDA_ERR_MISALIGNED = 3,  /* a pointer or the row stride breaks the 16-byte rule below */
+    KDA_ERR_CUDA = 4,        /* the launch failed; kda_last_error_string() has CUDA's message */
+    KDA_ERR_METADATA = 5     /* kda_validate_metadata found malformed metadata */
+} kda_status_t;
+
+typedef enum { KDA_ACT_NONE = 0, KDA_ACT_SILU = 1 } kda_activation_t;
+
+/*
+ * kda_packed_conv1d -- the conv, one launch.
+ *
+ * Device pointers, all owned by the caller:
+ *   x                 bf16 (tokens rows, x_row_stride elements apart); channels
+ *                     0..dim-1 of each row are the input (a column slice of the
+ *                     in_proj output, read in place). 16-byte aligned.
+ *   weight            fp32 (dim, 4), contiguous, weight[c*4 + j] multiplies row
+ *                     t-3+j. 16-byte aligned.
+ *   bias              fp32 (dim) or NULL for no bias. 16-byte aligned.
+ *   conv_states       fp32 (cache_lines, dim, 3), contiguous; index 2 is the most
+ *                     recent row. Read and updated in place. 16-byte aligned.
+ *   cache_indices     int32 [num_seqs]: the conv-state line of each sequence, or
+ *                     null_block_id for a padding sequence (computed with a zero
+ *                     history; its state is neither read nor written).
+ *   has_initial_state uint8/bool [num_seqs]: 0 = start from a zero history.
+ *   query_start_loc   int32 [num_seqs+1], non-decreasing, query_start_loc[num_seqs]
+ *                     <= tokens: sequence s owns token rows [qsl[s], qsl[s+1]).
+ *   out               bf16 (dim/part_dim, tokens, part_dim), dense; plane i holds
+ *                     channels [i*part_dim, (i+1)*part_dim). Rows no sequence owns
+ *                     are left as they were. 16-byte aligned.
+ * Scalars: x_row_stride >= dim and a multiple of 8 elements; part_dim a positive
+ * multiple of 64 dividing dim; activation a kda_activation_t; tokens and
+ * num_seqs >= 0.
+ *
+ * Returns KDA_OK after enqueueing the launch on `stream` (or without a launch when
+ * tokens == 0 or num_seqs == 0). Argument errors return without touching memory.
+ * The metadata (query_start_loc, cache_indices) is the caller's contract and is
+ * not checked on the device beyond clamping token rows to [0, tokens): a cache
+ * index outside [0, cache_lines) other than null_block_id, or two live sequences
+ * sharing a line, is undefined behaviour (kda_validate_metadata checks both).
+ * `out` must not overlap x or conv_states.
+ */
+kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
+                               int64_t part_dim, const float *weight, const float *bias,
+                               float *conv_states, const int32_t *cache_indices,
+                               const uint8_t *has_initial_state, const int32_t *query_start_loc,
+                               int64_t num_seqs, int64_t null_block_id, int activation, void *out,
+                               kda_stream_t stream);
+
+/*
+ * kda_packed_conv1d_preact_f32 -- the same conv without activation or rounding:
+ * `out` receives the FP32 accumulator (dim/part_dim, tokens, part_dim) and the conv
+ * state is updated exactly as by kda_packed_conv1d. Same arguments and rules as
+ * kda_packed_conv1d (there is no activation argument). For checking the FP32
+ * arithmetic bit for bit; not a hot path.
+ */
+kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, int64_t tokens,
+                                          int64_t dim, int64_t part_dim, const float *weight,
+                                          const float *bias, float *conv_states,
+                                          const int32_t *cache_indices,
+                                          const uint8_t *has_initial_state,
+                                          const int32_t *query_start_loc, int64_t num_seqs,
+                                          int64_t null_block_id, float *out, kda_stream_t stream);
+
+/*
+ * kda_packed_conv1d_check_args -- host only: the status kda_packed_conv1d would
+ * return for these arguments before launching (pointers are inspected for NULL and
+ * alignment only, never dereferenced). No CUDA call is made.
+ */
+kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, int64_t tokens,
+                                          int64_t dim, int64_t part_dim, const float *weight,
+                                          const float *bias, const float *conv_states,
+                                          const int32_t *cache_indices,
+                                          const uint8_t *has_initial_state,
+                                          const int32_t *query_start_loc, int64_t num_seqs,
+                                          int activation, const void *out);
+
+/*
+ * kda_packed_conv1d_launch_shape -- host only: the launch kda_packed_conv1d makes for
+ * these sizes. *ctas = thread blocks, *threads = threads per block, *chunk_tokens =
+ * tokens per program, *programs = token programs (ceil(tokens/chunk) + num_seqs).
+ * Returns KDA_OK, or KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED for bad sizes. When
+ * tokens == 0 or num_seqs == 0 all outputs are 0 (no launch).
+ */
+kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t part_dim,
+                                            int64_t num_seqs, int64_t *ctas, int32_t *threads,
+                                            int32_t *chunk_tokens, int64_t *programs);
+
+/*
+ * kda_validate_metadata -- host only, HOST pointers: checks query_start_loc
+ * (qsl[0] >= 0, non-decreasing, qsl[num_seqs] <= tokens) and cache_indices
+ * (each in [0, cache_lines) or equal to null_block_id; no line used by two
+ * sequences). Returns KDA_OK or KDA_ERR_METADATA with *bad_seq set to the first
+ * offending sequence (num_seqs for a bad final offset), or KDA_ERR_INVALID_ARG.
+ * bad_seq may be NULL.
+ */
+kda_status_t kda_validate_metadata(const int32_t *query_start_loc, const int32_t *cache_indices,
+                                   int64_t num_seqs, int64_t tokens, int64_t cache_lines,
+                                   int64_t null_block_id, int64_t *bad_seq);
+
+/*
+ * kda_epilogue_range -- the device epilogue of kda_packed_conv1d on its own:
+ * out[i] = bf16_round_nearest_even(act(f)) where f is the fp32 value whose bit
+ * pattern is first + i (wrapping mod 2^32), for i < count. Device `out` (uint16,
+ * count elements, 4-byte aligned), asynchronous on `stream`. For checking the
+ * activation and rounding over all fp32 inputs.
+ */
+kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, uint16_t *out,
+                                kda_stream_t stream);
+
+/* Static text for a status code. */
+const char *kda_status_string(kda_status_t status);
+
+/* The CUDA error text behind the calling thread's last KDA_ERR_CUDA ("" if none). */
+const char *kda_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_CONV_H_ */

@@ -1,0 +1,208 @@
+"""ctypes marshalling for libkdaconv.so (argument conversion only)."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_MISALIGNED = 3
+KDA_ERR_CUDA = 4
+KDA_ERR_METADATA = 5
+KDA_ACT_NONE = 0
+KDA_ACT_SILU = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    """A non-zero kda_status_t from the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(what)
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
+    P, I64, I32, C = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    conv = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64, I64]
+    handle.kda_packed_conv1d.argtypes = conv + [C, P, P]
+    handle.kda_packed_conv1d_preact_f32.argtypes = conv + [P, P]
+    handle.kda_packed_conv1d_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64,
+                                                    C, P]
+    handle.kda_packed_conv1d_launch_shape.argtypes = [
+        I64, I64, I64, I64, ctypes.POINTER(I64), ctypes.POINTER(I32), ctypes.POINTER(I32),
+        ctypes.POINTER(I64)]
+    handle.kda_validate_metadata.argtypes = [P, P, I64, I64, I64, I64, ctypes.POINTER(I64)]
+    handle.kda_epilogue_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, C, P, P]
+    for name in ("kda_packed_conv1d", "kda_packed_conv1d_preact_f32",
+                 "kda_packed_conv1d_check_args", "kda_packed_conv1d_launch_shape",
+                 "kda_validate_metadata", "kda_epilogue_range"):
+        getattr(handle, name).restype = C
+    handle.kda_status_string.argtypes = [C]
+    handle.kda_status_string.restype = ctypes.c_char_p
+    handle.kda_last_error_string.argtypes = []
+    handle.kda_last_error_string.restype = ctypes.c_char_p
+    return handle
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it first (linear_attention_prefill_varlen_gb300."
+                    "_build.build(), or __graft_entry__.build()); there is no CPU fallback")
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != KDA_OK:
+        h = lib()
+        what = h.kda_status_string(status).decode()
+        if status == KDA_ERR_CUDA:
+            what += ": " + h.kda_last_error_string().decode()
+        raise KdaError(status, what)
+
+
+def _ptr(t) -> int | None:
+    """Device (or host) address of a tensor, an int address, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def kda_packed_conv1d(x, x_row_stride: int, tokens: int, dim: int, part_dim: int, weight, bias,
+                      conv_states, cache_indices, has_initial_state, query_start_loc,
+                      num_seqs: int, null_block_id: int, activation: int, out,
+                      stream=None) -> None:
+    """C-ABI kda_packed_conv1d.  Tensors (or raw device addresses) are passed
+    by pointer exactly as given; the call is asynchronous on `stream`
+    (default: torch's current stream)."""
+    _check(lib().kda_packed_conv1d(
+        _ptr(x), x_row_stride, tokens, dim, part_dim, _ptr(weight), _ptr(bias),
+        _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
+        num_seqs, null_block_id, activation, _ptr(out), _stream(stream)))
+
+
+def kda_packed_conv1d_preact_f32(x, x_row_stride: int, tokens: int, dim: int, part_dim: int,
+                                 weight, bias, conv_states, cache_indices, has_initial_state,
+                                 query_start_loc, num_seqs: int, null_block_id: int, out,
+                                 stream=None) -> None:
+    """C-ABI kda_packed_conv1d_preact_f32: FP32 accumulators into `out`."""
+    _check(lib().kda_packed_conv1d_preact_f32(
+        _ptr(x), x_row_stride, tokens, dim, part_dim, _ptr(weight), _ptr(bias),
+        _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
+        num_seqs, null_block_id, _ptr(out), _stream(stream)))
+
+
+def check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
+               cache_indices, has_initial_state, query_start_loc, num_seqs, activation,
+               out) -> int:
+    """Host-only argument check (never dereferences a pointer); returns the status."""
+    return lib().kda_packed_conv1d_check_args(
+        _ptr(x), x_row_stride, tokens, dim, part_dim, _ptr(weight), _ptr(bias),
+        _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
+        num_seqs, activation, _ptr(out))
+
+
+def launch_shape(tokens: int, dim: int, part_dim: int, num_seqs: int) -> dict:
+    """The launch the library makes for these sizes (host only)."""
+    ctas, programs = ctypes.c_int64(), ctypes.c_int64()
+    threads, chunk = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().kda_packed_conv1d_launch_shape(tokens, dim, part_dim, num_seqs,
+                                                ctypes.byref(ctas), ctypes.byref(threads),
+                                                ctypes.byref(chunk), ctypes.byref(programs)))
+    return {"ctas": ctas.value, "threads": threads.value, "chunk": chunk.value,
+            "programs": programs.value}
+
+
+def validate_metadata(query_start_loc, cache_indices, tokens: int, cache_lines: int,
+                      null_block_id: int) -> tuple[int, int]:
+    """Host-side metadata check.  Accepts CPU or CUDA int32 tensors (CUDA ones
+    are copied to the host, which synchronises).  Returns (status, bad seq)."""
+    qsl = torch.as_tensor(query_start_loc).to("cpu", torch.int32).contiguous()
+    ci = torch.as_tensor(cache_indices).to("cpu", torch.int32).contiguous()
+    bad = ctypes.c_int64(-1)
+    st = lib().kda_validate_metadata(qsl.data_ptr(), ci.data_ptr(), qsl.numel() - 1, tokens,
+                                     cache_lines, null_block_id, ctypes.byref(bad))
+    return st, bad.value
+
+
+def epilogue_range(first: int, count: int, activation: int, out, stream=None) -> None:
+    """C-ABI kda_epilogue_range into a device uint16/int16 tensor."""
+    _check(lib().kda_epilogue_range(first, count, activation, _ptr(out), _stream(stream)))
+
+
+_SILU_NAMES = ("silu", "swish", True)
+
+
+def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
+                                   conv_states: torch.Tensor, part_dim: int) -> bool:
+    """Whether packed_causal_conv1d_fn takes these inputs on this library: bf16 x
+    on CUDA with unit channel stride and 16-byte aligned rows, FP32 weight
+    (dim, 4) and contiguous FP32 conv_states (lines, dim, 3), part_dim a
+    multiple of 64 dividing dim (the page's predicate narrowed to what the
+    kernel reads)."""
+    return (
+        x.is_cuda and x.dim() == 2 and x.stride(1) == 1 and x.dtype == torch.bfloat16
+        and x.stride(0) % 8 == 0 and x.data_ptr() % 16 == 0
+        and weight.dtype == torch.float32 and weight.dim() == 2 and weight.is_contiguous()
+        and weight.size(0) == x.size(1) and weight.size(1) == 4
+        and conv_states.dtype == torch.float32 and conv_states.dim() == 3
+        and conv_states.is_contiguous() and conv_states.size(1) == x.size(1)
+        and conv_states.size(2) == 3
+        and part_dim > 0 and part_dim % 64 == 0 and x.size(1) % part_dim == 0
+    )
+
+
+def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None,
+                            conv_states: torch.Tensor, query_start_loc: torch.Tensor,
+                            cache_indices: torch.Tensor, has_initial_state: torch.Tensor,
+                            part_dim: int, activation="silu", null_block_id: int | None = None,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Varlen causal depthwise conv of x (tokens, dim), dim = parts x part_dim.
+
+    Returns (dim // part_dim, tokens, part_dim) bf16; conv_states is updated in
+    place.  `activation` in ("silu", "swish", True) selects SiLU, anything else
+    none.  `null_block_id=None` disables padding detection (the library gets a
+    value no cache index can hold).  `out` may be given to avoid the
+    allocation."""
+    tokens, dim = x.shape
+    num_seqs = query_start_loc.numel() - 1
+    if out is None:
+        out = torch.empty((dim // part_dim, tokens, part_dim), dtype=x.dtype, device=x.device)
+    if has_initial_state.dtype != torch.uint8 and has_initial_state.dtype != torch.bool:
+        raise TypeError("has_initial_state must be bool or uint8")
+    act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
+    null = -(2 ** 62) if null_block_id is None else int(null_block_id)
+    kda_packed_conv1d(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
+                      cache_indices, has_initial_state, query_start_loc, max(num_seqs, 0), null,
+                      act, out, stream)
+    return out

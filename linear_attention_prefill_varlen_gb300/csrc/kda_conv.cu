@@ -1,0 +1,611 @@
+// Packed varlen causal depthwise conv1d (width 4) for GB300 / sm_103a.
+//
+// The operation is the one the vLLM page "vllm.models.kimi_k3.nvidia.ops.kda_conv"
+// describes (module docstring and packed_causal_conv1d_fn): a row-strided bf16
+// x (tokens, dim) is read in place, each channel is convolved causally over its
+// sequence with 4 FP32 taps (history rows from an FP32 paged conv state), SiLU is
+// optional, and the result is rounded to bf16 (nearest even) into dense
+// (tokens, part_dim) planes.  The exact per-element arithmetic is spelled out in
+// include/kda_conv.h.
+//
+// Design (memory-bound stencil, no contraction, so no tensor cores):
+//   * grid = token programs x channel blocks, linearised with the channel block
+//     fastest so that neighbouring CTAs stream neighbouring columns of the same
+//     rows.  A token program p belongs to sequence s with f(s) <= p < f(s+1),
+//     f(s) = floor(qsl[s] / chunk) + s; each sequence owns at least
+//     ceil(len / chunk) programs and the total is at most ceil(tokens/chunk) +
+//     num_seqs (the bound the page's launch uses).  Each warp finds s with a
+//     radix-32 search over query_start_loc (one coalesced 32-candidate probe per
+//     level), so there is no host-side chunk table and the grid depends only on
+//     tokens and num_seqs (graph-safe).
+//   * a thread owns VEC channels (one 16- or 8-byte vector of a row) and walks
+//     the chunk's rows in order: 3 history rows stay in registers as FP32, the
+//     next U rows are loaded one step ahead into a register queue, and every
+//     row is 4 FMAs per channel in a fixed order, the activation, a packed RNE
+//     conversion and one vector store into its plane.
+//   * the first chunk of a sequence reads its conv state and, in the same
+//     thread, writes the updated state (the sequence's last 3 rows, or the
+//     shifted old history for sequences shorter than 3), so there is exactly
+//     one reader and one writer per state line and no ordering between CTAs.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_conv.h"
+
+namespace {
+
+struct Params {
+    const uint16_t *x;
+    int64_t x_row_stride;  // elements
+    int tokens;
+    int dim;
+    int part_dim;
+    int num_seqs;
+    const float *weight;
+    const float *bias;
+    float *conv_states;
+    const int32_t *cache_indices;
+    const uint8_t *has_initial_state;
+    const int32_t *qsl;
+    int64_t null_block_id;
+    void *out;
+    int64_t plane_stride;  // tokens * part_dim elements
+    int chunk;             // tokens per program (>= 4)
+    int col_blocks;        // channel blocks per token program
+    int search_steps;      // radix-32 levels: smallest s with 32^s >= num_seqs
+    int search_top;        // 32^(search_steps - 1)
+};
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+// One row vector of VEC bf16 channels, as VEC/2 32-bit words (channel 2i in the
+// low half of word i).  Streaming load: read once, keep out of L1.
+template <int VEC>
+__device__ __forceinline__ void load_row(const uint16_t *p, uint32_t (&w)[VEC / 2]) {
+    if constexpr (VEC == 8) {
+        asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+            : "l"(p));
+    } else {
+        static_assert(VEC == 4, "VEC must be 4 or 8");
+        asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+            : "=r"(w[0]), "=r"(w[1])
+            : "l"(p));
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void zero_row(uint32_t (&w)[VEC / 2]) {
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) w[i] = 0u;
+}
+
+// bf16 -> fp32 is exact: a bf16 is the upper half of an fp32 bit pattern.
+template <int VEC>
+__device__ __forceinline__ void widen(const uint32_t (&w)[VEC / 2], float (&f)[VEC]) {
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Two fp32 -> one word of two bf16, round to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    return u;
+}
+
+// SiLU in FP32: a / (1 + exp(-a)), IEEE division.
+__device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + expf(-a)); }
+
+template <int VEC>
+__device__ __forceinline__ void store_bf16_row(uint16_t *p, const float (&y)[VEC]) {
+    uint32_t w[VEC / 2];
+#pragma unroll
+    for (int i = 0; i < VEC / 2; ++i) w[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
+    if constexpr (VEC == 8) {
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                     "r"(w[2]), "r"(w[3])
+                     : "memory");
+    } else {
+        asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
+                     : "memory");
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_f32_row(float *p, const float (&y)[VEC]) {
+#pragma unroll
+    for (int i = 0; i < VEC / 4; ++i) {
+        reinterpret_cast<float4 *>(p)[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2],
+                                                       y[4 * i + 3]);
+    }
+}
+
+// The sequence that owns token program `prog`, or -1 if the program is idle
+// before the first sequence.  Must be called by all 32 lanes of a warp.
+__device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane) {
+    int base = 0;
+    int stride = p.search_top;
+    for (int level = 0; level < p.search_steps; ++level) {
+        const int idx = base + lane * stride;
+        bool ok = false;
+        if (idx < p.num_seqs) ok = (__ldg(p.qsl + idx) / p.chunk + idx) <= prog;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
+        if (m == 0u) return -1;
+        base += (__popc(m) - 1) * stride;
+        stride >>= 5;
+    }
+    return base;
+}
+
+// ---------------------------------------------------------------------------
+// The conv kernel
+// ---------------------------------------------------------------------------
+
+template <int VEC, int U, bool kPreact, bool kSilu, bool kBias>
+__global__ void __launch_bounds__(256) kda_packed_conv1d_kernel(const Params p) {
+    const int lane = threadIdx.x & 31;
+    const int prog = blockIdx.x / p.col_blocks;
+    const int cb = blockIdx.x - prog * p.col_blocks;
+
+    const int s = find_sequence(p, prog, lane);
+    if (s < 0) return;
+    const int q0 = __ldg(p.qsl + s);
+    const int f_s = q0 / p.chunk + s;
+    if (f_s > prog) return;
+    // Clamp the sequence to [0, tokens) so that malformed offsets never read or
+    // write outside x / out.
+    const int a = max(q0, 0);
+    const int e = min(__ldg(p.qsl + s + 1), p.tokens);
+    const int k = prog - f_s;
+    const int64_t t0_wide = (int64_t)a + (int64_t)k * p.chunk;
+    if (t0_wide >= e) return;
+    const int t0 = (int)t0_wide;
+    const int t1 = min(t0 + p.chunk, e);
+
+    const int c = (cb * (int)blockDim.x + (int)threadIdx.x) * VEC;
+    if (c >= p.dim) return;
+
+    // Taps and bias of this thread's channels.
+    float w[VEC][4];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(p.weight) + (c + v));
+        w[v][0] = q.x;
+        w[v][1] = q.y;
+        w[v][2] = q.z;
+        w[v][3] = q.w;
+    }
+    float bias[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC / 4; ++i) {
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (kBias) q = __ldg(reinterpret_cast<const float4 *>(p.bias + c) + i);
+        bias[4 * i] = q.x;
+        bias[4 * i + 1] = q.y;
+        bias[4 * i + 2] = q.z;
+        bias[4 * i + 3] = q.w;
+    }
+
+    const uint16_t *xcol = p.x + c;
+    const int64_t xs = p.x_row_stride;
+
+    // History rows -3, -2, -1 relative to t0 (h0 oldest), in FP32.
+    float h0[VEC], h1[VEC], h2[VEC];
+    if (k == 0) {
+        const int64_t line = __ldg(p.cache_indices + s);
+        const bool live = line != p.null_block_id;
+        float st[3 * VEC];
+#pragma unroll
+        for (int i = 0; i < 3 * VEC; ++i) st[i] = 0.0f;
+        float4 *sp = reinterpret_cast<float4 *>(p.conv_states + (line * p.dim + c) * 3);
+        if (live && __ldg(p.has_initial_state + s) != 0) {
+#pragma unroll
+            for (int i = 0; i < 3 * VEC / 4; ++i) {
+                const float4 q = sp[i];
+                st[4 * i] = q.x;
+                st[4 * i + 1] = q.y;
+                st[4 * i + 2] = q.z;
+                st[4 * i + 3] = q.w;
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            h0[v] = st[3 * v];
+            h1[v] = st[3 * v + 1];
+            h2[v] = st[3 * v + 2];
+        }
+        if (live) {
+            // The updated state: the last 3 rows of [history ; rows a .. e-1].
+            const int len = e - a;
+            float ns[3][VEC];
+#pragma unroll
+            for (int r = 0; r < 3; ++r) {
+                const int row = len - 3 + r;
+                if (row >= 0) {
+                    uint32_t raw[VEC / 2];
+                    load_row<VEC>(xcol + (int64_t)(a + row) * xs, raw);
+                    widen<VEC>(raw, ns[r]);
+                } else {
+                    // history index row + 3 = len + r, which is 1 or 2 here
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) ns[r][v] = (len + r == 1) ? h1[v] : h2[v];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 3 * VEC / 4; ++i) {
+                float o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int flat = 4 * i + j;  // = 3 * channel + state index
+                    o[j] = ns[flat % 3][flat / 3];
+                }
+                sp[i] = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    } else {
+        uint32_t raw[VEC / 2];
+        load_row<VEC>(xcol + (int64_t)(t0 - 3) * xs, raw);
+        widen<VEC>(raw, h0);
+        load_row<VEC>(xcol + (int64_t)(t0 - 2) * xs, raw);
+        widen<VEC>(raw, h1);
+        load_row<VEC>(xcol + (int64_t)(t0 - 1) * xs, raw);
+        widen<VEC>(raw, h2);
+    }
+
+    const int plane = c / p.part_dim;
+    const int col = c - plane * p.part_dim;
+    const int64_t out_base = (int64_t)plane * p.plane_stride + col;
+
+    // Register queue: rows t .. t+U-1 are in `cur` while rows t+U .. t+2U-1 load.
+    uint32_t cur[U][VEC / 2];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (t0 + u < t1)
+            load_row<VEC>(xcol + (int64_t)(t0 + u) * xs, cur[u]);
+        else
+            zero_row<VEC>(cur[u]);
+    }
+    for (int t = t0; t < t1; t += U) {
+        uint32_t nxt[U][VEC / 2];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int r = t + U + u;
+            if (r < t1)
+                load_row<VEC>(xcol + (int64_t)r * xs, nxt[u]);
+            else
+                zero_row<VEC>(nxt[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            float xv[VEC];
+            widen<VEC>(cur[u], xv);
+            float y[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                float acc = kBias ? bias[v] : 0.0f;
+                acc = __fmaf_rn(h0[v], w[v][0], acc);
+                acc = __fmaf_rn(h1[v], w[v][1], acc);
+                acc = __fmaf_rn(h2[v], w[v][2], acc);
+                acc = __fmaf_rn(xv[v], w[v][3], acc);
+                y[v] = kSilu ? silu_f32(acc) : acc;
+                h0[v] = h1[v];
+                h1[v] = h2[v];
+                h2[v] = xv[v];
+            }
+            if (t + u < t1) {
+                const int64_t o = out_base + (int64_t)(t + u) * p.part_dim;
+                if constexpr (kPreact)
+                    store_f32_row<VEC>(static_cast<float *>(p.out) + o, y);
+                else
+                    store_bf16_row<VEC>(static_cast<uint16_t *>(p.out) + o, y);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int i = 0; i < VEC / 2; ++i) cur[u][i] = nxt[u][i];
+        }
+    }
+}
+
+// The epilogue alone, over consecutive fp32 bit patterns (two per thread step,
+// through the same pack as the conv kernel).
+template <bool kSilu>
+__global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first, uint64_t count,
+                                                                 uint16_t *out) {
+    const uint64_t step = 2ull * gridDim.x * blockDim.x;
+    for (uint64_t i = 2ull * (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x); i < count;
+         i += step) {
+        float lo = __uint_as_float(first + (uint32_t)i);
+        float hi = __uint_as_float(first + (uint32_t)(i + 1));
+        if (kSilu) {
+            lo = silu_f32(lo);
+            hi = silu_f32(hi);
+        }
+        const uint32_t w = pack_bf16x2(lo, hi);
+        if (i + 1 < count)
+            *reinterpret_cast<uint32_t *>(out + i) = w;
+        else
+            out[i] = (uint16_t)(w & 0xFFFFu);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+thread_local char g_last_error[256] = "";
+
+constexpr int kVec = 8;
+constexpr int kUnroll = 8;
+constexpr int kThreads = 128;
+constexpr int kChunk = 64;
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+kda_status_t check_sizes(int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
+                         int64_t num_seqs) {
+    if (tokens < 0 || dim < 0 || num_seqs < 0 || part_dim <= 0) return KDA_ERR_INVALID_ARG;
+    if (tokens > INT32_MAX || dim > INT32_MAX / 4 || num_seqs > (int64_t(1) << 30))
+        return KDA_ERR_INVALID_ARG;
+    if (x_row_stride < dim) return KDA_ERR_INVALID_ARG;
+    if (part_dim % 64 != 0 || dim % part_dim != 0) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
+                        int64_t part_dim, const float *weight, const float *bias,
+                        const float *conv_states, const int32_t *cache_indices,
+                        const uint8_t *has_initial_state, const int32_t *query_start_loc,
+                        int64_t num_seqs, int activation, const void *out) {
+    kda_status_t st = check_sizes(x_row_stride, tokens, dim, part_dim, num_seqs);
+    if (st != KDA_OK) return st;
+    if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
+    if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;  // nothing is touched
+    if (!x || !weight || !conv_states || !cache_indices || !has_initial_state ||
+        !query_start_loc || !out)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned16(x) || x_row_stride % 8 != 0 || !aligned16(weight) ||
+        (bias && !aligned16(bias)) || !aligned16(conv_states) || !aligned16(out))
+        return KDA_ERR_MISALIGNED;
+    return KDA_OK;
+}
+
+struct Shape {
+    int64_t ctas;
+    int threads;
+    int chunk;
+    int64_t programs;
+    int col_blocks;
+};
+
+Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs) {
+    Shape sh{};
+    sh.threads = kThreads;
+    sh.chunk = kChunk;
+    sh.programs = (tokens + sh.chunk - 1) / sh.chunk + num_seqs;
+    const int64_t per_block = (int64_t)kVec * sh.threads;
+    sh.col_blocks = (int)((dim + per_block - 1) / per_block);
+    sh.ctas = sh.programs * sh.col_blocks;
+    return sh;
+}
+
+template <bool kPreact, bool kSilu, bool kBias>
+void launch(const Params &p, const Shape &sh, cudaStream_t stream) {
+    kda_packed_conv1d_kernel<kVec, kUnroll, kPreact, kSilu, kBias>
+        <<<(unsigned)sh.ctas, sh.threads, 0, stream>>>(p);
+}
+
+kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
+                 int64_t part_dim, const float *weight, const float *bias, float *conv_states,
+                 const int32_t *cache_indices, const uint8_t *has_initial_state,
+                 const int32_t *query_start_loc, int64_t num_seqs, int64_t null_block_id,
+                 int activation, void *out, bool preact, kda_stream_t stream) {
+    kda_status_t st = check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
+                                 cache_indices, has_initial_state, query_start_loc, num_seqs,
+                                 activation, out);
+    if (st != KDA_OK) return st;
+    if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;
+
+    const Shape sh = launch_shape(tokens, dim, num_seqs);
+    if (sh.ctas > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    Params p;
+    p.x = static_cast<const uint16_t *>(x);
+    p.x_row_stride = x_row_stride;
+    p.tokens = (int)tokens;
+    p.dim = (int)dim;
+    p.part_dim = (int)part_dim;
+    p.num_seqs = (int)num_seqs;
+    p.weight = weight;
+    p.bias = bias;
+    p.conv_states = conv_states;
+    p.cache_indices = cache_indices;
+    p.has_initial_state = has_initial_state;
+    p.qsl = query_start_loc;
+    p.null_block_id = null_block_id;
+    p.out = out;
+    p.plane_stride = tokens * part_dim;
+    p.chunk = sh.chunk;
+    p.col_blocks = sh.col_blocks;
+    int steps = 0;
+    int64_t reach = 1;
+    while (reach < num_seqs) {
+        reach *= 32;
+        ++steps;
+    }
+    p.search_steps = steps;
+    p.search_top = steps > 0 ? (int)(reach / 32) : 1;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool silu = activation == KDA_ACT_SILU;
+    if (preact) {
+        if (bias)
+            launch<true, false, true>(p, sh, s);
+        else
+            launch<true, false, false>(p, sh, s);
+    } else if (silu) {
+        if (bias)
+            launch<false, true, true>(p, sh, s);
+        else
+            launch<false, true, false>(p, sh, s);
+    } else {
+        if (bias)
+            launch<false, false, true>(p, sh, s);
+        else
+            launch<false, false, false>(p, sh, s);
+    }
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
+                 cudaGetErrorString(err));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
+                               int64_t part_dim, const float *weight, const float *bias,
+                               float *conv_states, const int32_t *cache_indices,
+                               const uint8_t *has_initial_state, const int32_t *query_start_loc,
+                               int64_t num_seqs, int64_t null_block_id, int activation, void *out,
+                               kda_stream_t stream) {
+    return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
+               has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
+               false, stream);
+}
+
+kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, int64_t tokens,
+                                          int64_t dim, int64_t part_dim, const float *weight,
+                                          const float *bias, float *conv_states,
+                                          const int32_t *cache_indices,
+                                          const uint8_t *has_initial_state,
+                                          const int32_t *query_start_loc, int64_t num_seqs,
+                                          int64_t null_block_id, float *out, kda_stream_t stream) {
+    return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
+               has_initial_state, query_start_loc, num_seqs, null_block_id, KDA_ACT_NONE, out,
+               true, stream);
+}
+
+kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, int64_t tokens,
+                                          int64_t dim, int64_t part_dim, const float *weight,
+                                          const float *bias, const float *conv_states,
+                                          const int32_t *cache_indices,
+                                          const uint8_t *has_initial_state,
+                                          const int32_t *query_start_loc, int64_t num_seqs,
+                                          int activation, const void *out) {
+    return check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
+                      cache_indices, has_initial_state, query_start_loc, num_seqs, activation,
+                      out);
+}
+
+kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t part_dim,
+                                            int64_t num_seqs, int64_t *ctas, int32_t *threads,
+                                            int32_t *chunk_tokens, int64_t *programs) {
+    kda_status_t st = check_sizes(dim, tokens, dim, part_dim, num_seqs);
+    if (st != KDA_OK) return st;
+    Shape sh{};
+    if (tokens > 0 && num_seqs > 0 && dim > 0) sh = launch_shape(tokens, dim, num_seqs);
+    if (ctas) *ctas = sh.ctas;
+    if (threads) *threads = sh.threads;
+    if (chunk_tokens) *chunk_tokens = sh.chunk;
+    if (programs) *programs = sh.programs;
+    return KDA_OK;
+}
+
+kda_status_t kda_validate_metadata(const int32_t *query_start_loc, const int32_t *cache_indices,
+                                   int64_t num_seqs, int64_t tokens, int64_t cache_lines,
+                                   int64_t null_block_id, int64_t *bad_seq) {
+    int64_t dummy;
+    int64_t *bad = bad_seq ? bad_seq : &dummy;
+    *bad = -1;
+    if (num_seqs < 0 || tokens < 0 || cache_lines < 0) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return KDA_OK;
+    if (!query_start_loc || !cache_indices) return KDA_ERR_INVALID_ARG;
+    if (query_start_loc[0] < 0) {
+        *bad = 0;
+        return KDA_ERR_METADATA;
+    }
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        if (query_start_loc[s + 1] < query_start_loc[s]) {
+            *bad = s;
+            return KDA_ERR_METADATA;
+        }
+    }
+    if (query_start_loc[num_seqs] > tokens) {
+        *bad = num_seqs;
+        return KDA_ERR_METADATA;
+    }
+    // A line may serve one sequence only: mark lines in a byte map.
+    unsigned char *seen = nullptr;
+    if (cache_lines > 0) {
+        seen = static_cast<unsigned char *>(calloc((size_t)cache_lines, 1));
+        if (!seen) return KDA_ERR_INVALID_ARG;
+    }
+    kda_status_t st = KDA_OK;
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        const int64_t line = cache_indices[s];
+        if (line == null_block_id) continue;
+        if (line < 0 || line >= cache_lines || seen[line]) {
+            *bad = s;
+            st = KDA_ERR_METADATA;
+            break;
+        }
+        seen[line] = 1;
+    }
+    free(seen);
+    return st;
+}
+
+kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, uint16_t *out,
+                                kda_stream_t stream) {
+    if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
+    if (count == 0) return KDA_OK;
+    if (!out) return KDA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0) return KDA_ERR_MISALIGNED;
+    const uint64_t pairs = (count + 1) / 2;
+    const unsigned threads = 256;
+    const uint64_t want = (pairs + threads - 1) / threads;
+    const unsigned blocks = (unsigned)(want < 152ull * 64 ? want : 152ull * 64);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (activation == KDA_ACT_SILU)
+        kda_epilogue_range_kernel<true><<<blocks, threads, 0, s>>>(first, count, out);
+    else
+        kda_epilogue_range_kernel<false><<<blocks, threads, 0, s>>>(first, count, out);
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
+                 cudaGetErrorString(err));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+const char *kda_status_string(kda_status_t status) {
+    switch (status) {
+        case KDA_OK: return "ok";
+        case KDA_ERR_INVALID_ARG: return "invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "unsupported shape (part_dim % 64 or dim % part_dim)";
+        case KDA_ERR_MISALIGNED: return "misaligned pointer or row stride (16-byte rule)";
+        case KDA_ERR_CUDA: return "CUDA launch error";
+        case KDA_ERR_METADATA: return "malformed metadata";
+    }
+    return "unknown status";
+}
+
+const char *kda_last_error_string(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, and its host-only logic (argument checks, launch shape, metadata
+validation, empty calls) behaves as documented.  No kernel is launched."""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda_conv.h")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from linear_attention_prefill_varlen_gb300 import _binding, _build
+
+    _build.build()
+    _binding.lib()
+    return _binding
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_conv_entry_point():
+    names = declared_functions()
+    assert "kda_packed_conv1d" in names
+    assert len(names) >= 8, names
+
+
+def test_library_exports_every_declared_symbol(kda):
+    handle = ctypes.CDLL(kda.lib_path())
+    missing = [n for n in declared_functions() if not hasattr(handle, n)]
+    assert not missing, missing
+
+
+A16 = 1 << 20  # a fake 16-byte aligned address: never dereferenced by the host checks
+
+
+def good_args(**over):
+    args = dict(x=A16, x_row_stride=6400, tokens=100, dim=4608, part_dim=1536, weight=A16,
+                bias=A16, conv_states=A16, cache_indices=A16, has_initial_state=A16,
+                query_start_loc=A16, num_seqs=3, activation=1, out=A16)
+    args.update(over)
+    return args
+
+
+def check(kda, **over) -> int:
+    a = good_args(**over)
+    return kda.check_args(a["x"], a["x_row_stride"], a["tokens"], a["dim"], a["part_dim"],
+                          a["weight"], a["bias"], a["conv_states"], a["cache_indices"],
+                          a["has_initial_state"], a["query_start_loc"], a["num_seqs"],
+                          a["activation"], a["out"])
+
+
+@pytest.mark.parametrize("over,status", [
+    ({}, 0),
+    ({"bias": None}, 0),
+    ({"activation": 0}, 0),
+    ({"activation": 2}, 1),
+    ({"tokens": -1}, 1),
+    ({"num_seqs": -1}, 1),
+    ({"x_row_stride": 4600}, 1),
+    ({"part_dim": 0}, 1),
+    ({"part_dim": 1000}, 2),
+    ({"part_dim": 1024}, 2),  # multiple of 64 that does not divide dim
+    ({"x": None}, 1),
+    ({"weight": None}, 1),
+    ({"conv_states": None}, 1),
+    ({"cache_indices": None}, 1),
+    ({"has_initial_state": None}, 1),
+    ({"query_start_loc": None}, 1),
+    ({"out": None}, 1),
+    ({"x": A16 + 2}, 3),
+    ({"x_row_stride": 6404}, 3),
+    ({"weight": A16 + 4}, 3),
+    ({"bias": A16 + 8}, 3),
+    ({"conv_states": A16 + 4}, 3),
+    ({"out": A16 + 2}, 3),
+    ({"tokens": 0, "x": None, "out": None}, 0),  # empty: nothing is touched
+    ({"num_seqs": 0, "query_start_loc": None}, 0),
+])
+def test_argument_checks(kda, over, status):
+    assert check(kda, **over) == status
+
+
+def test_entry_point_rejects_before_any_cuda_call(kda):
+    """Rejected and empty calls return without touching CUDA (safe without a GPU)."""
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_packed_conv1d(A16, 6400, 100, 4608, 1000, A16, A16, A16, A16, A16, A16, 3, -1, 1,
+                              A16, stream=0)
+    assert e.value.status == kda.KDA_ERR_UNSUPPORTED
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_packed_conv1d(A16 + 2, 6400, 100, 4608, 1536, A16, A16, A16, A16, A16, A16, 3, -1,
+                              1, A16, stream=0)
+    assert e.value.status == kda.KDA_ERR_MISALIGNED
+    kda.kda_packed_conv1d(A16, 6400, 0, 4608, 1536, A16, A16, A16, A16, A16, A16, 3, -1, 1, A16,
+                          stream=0)
+    kda.kda_packed_conv1d(A16, 6400, 5, 4608, 1536, A16, A16, A16, A16, A16, A16, 0, -1, 1, A16,
+                          stream=0)
+
+
+def test_status_strings(kda):
+    h = kda.lib()
+    for s in range(6):
+        assert h.kda_status_string(s)
+    assert h.kda_status_string(99) == b"unknown status"
+
+
+@pytest.mark.parametrize("tokens,num_seqs", [(16384, 1), (2430, 8), (18003, 1280), (64, 1),
+                                             (1, 1), (100, 400)])
+def test_launch_shape_bound(kda, tokens, num_seqs):
+    """Programs = ceil(tokens / chunk) + num_seqs: every sequence adds at most
+    one partial chunk (the bound of the page's launch)."""
+    sh = kda.launch_shape(tokens, 4608, 1536, num_seqs)
+    assert sh["chunk"] >= 4
+    assert sh["programs"] == -(-tokens // sh["chunk"]) + num_seqs
+    assert sh["ctas"] % sh["programs"] == 0
+    assert sh["ctas"] // sh["programs"] * sh["threads"] * 8 >= 4608
+
+
+def test_program_map_covers_every_chunk_once(kda):
+    """The map f(s) = floor(qsl[s] / chunk) + s gives each sequence at least
+    ceil(len / chunk) programs inside the grid (host model of the device map)."""
+    rng = np.random.default_rng(5)
+    for trial in range(200):
+        n = int(rng.integers(1, 60))
+        lens = rng.integers(0, 300, size=n)
+        qsl = np.concatenate([[int(rng.integers(0, 50))], lens]).cumsum()
+        tokens = int(qsl[-1] + rng.integers(0, 20))
+        sh = kda.launch_shape(tokens, 256, 128, n)
+        chunk = sh["chunk"]
+        f = qsl[:-1] // chunk + np.arange(n)
+        f_next = np.append(f[1:], sh["programs"])
+        assert (np.diff(f) >= 1).all()
+        assert (f_next - f >= -(-lens // chunk)).all()
+        assert f[-1] + -(-lens[-1] // chunk) <= sh["programs"]
+
+
+def test_validate_metadata(kda):
+    ok = kda.validate_metadata(torch.tensor([0, 2, 5]), torch.tensor([0, 1]), 8, 4, -1)
+    assert ok == (0, -1)
+    cases = [
+        ([0, 6, 5], [0, 1], 1),
+        ([-1, 2, 5], [0, 1], 0),
+        ([0, 2, 9], [0, 1], 2),
+        ([0, 2, 5], [0, 4], 1),
+        ([0, 2, 5], [-2, 1], 0),
+        ([0, 2, 5], [1, 1], 1),
+    ]
+    for qsl, ci, bad in cases:
+        st, where = kda.validate_metadata(torch.tensor(qsl), torch.tensor(ci), 8, 4, -1)
+        assert st == kda.KDA_ERR_METADATA and where == bad, (qsl, ci, st, where)
+    assert kda.validate_metadata(torch.tensor([0, 2, 5]), torch.tensor([-1, -1]), 8, 4, -1)[0] == 0
