@@ -131,15 +131,18 @@ kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, i
                                           int activation, const void *out);
 
 /*
- * kda_packed_conv1d_launch_shape -- host only: the launch kda_packed_conv1d makes for
- * these sizes. *ctas = thread blocks, *threads = threads per block, *chunk_tokens =
- * tokens per program, *programs = token programs (ceil(tokens/chunk) + num_seqs).
- * Returns KDA_OK, or KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED for bad sizes. When
- * tokens == 0 or num_seqs == 0 all outputs are 0 (no launch).
+ * kda_packed_conv1d_launch_shape -- the launch kda_packed_conv1d makes for these
+ * sizes on a GPU with sm_count SMs (sm_count = 0: the current device, which makes
+ * one CUDA attribute query; a positive sm_count makes no CUDA call). *ctas = thread
+ * blocks, *threads = threads per block, *chunk_tokens = tokens per program,
+ * *programs = token programs (ceil(tokens/chunk) + num_seqs). Returns KDA_OK, or
+ * KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED for bad sizes. When tokens == 0 or
+ * num_seqs == 0 all outputs are 0 (no launch). Output pointers may be NULL.
  */
 kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t part_dim,
-                                            int64_t num_seqs, int64_t *ctas, int32_t *threads,
-                                            int32_t *chunk_tokens, int64_t *programs);
+                                            int64_t num_seqs, int32_t sm_count, int64_t *ctas,
+                                            int32_t *threads, int32_t *chunk_tokens,
+                                            int64_t *programs);
 
 /*
  * kda_validate_metadata -- host only, HOST pointers: checks query_start_loc
@@ -154,11 +157,12 @@ kda_status_t kda_validate_metadata(const int32_t *query_start_loc, const int32_t
                                    int64_t null_block_id, int64_t *bad_seq);
 
 /*
- * kda_epilogue_range -- the device epilogue of kda_packed_conv1d on its own:
- * out[i] = bf16_round_nearest_even(act(f)) where f is the fp32 value whose bit
- * pattern is first + i (wrapping mod 2^32), for i < count. Device `out` (uint16,
- * count elements, 4-byte aligned), asynchronous on `stream`. For checking the
- * activation and rounding over all fp32 inputs.
+ * kda_epilogue_range -- the device epilogue of kda_packed_conv1d on its own, for
+ * checking it over all fp32 inputs. out[i] = bf16_round_nearest_even(act(f)), where
+ * f is the fp32 value whose bit pattern is first + i (wrapping mod 2^32), for
+ * i < count, through the same device functions as the conv kernel.
+ * activation: KDA_ACT_NONE or KDA_ACT_SILU. Device `out` (uint16, count
+ * elements, 16-byte aligned), asynchronous on `stream`.
  */
 kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, uint16_t *out,
                                 kda_stream_t stream);

@@ -43,7 +43,7 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     handle.kda_packed_conv1d_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64,
                                                     C, P]
     handle.kda_packed_conv1d_launch_shape.argtypes = [
-        I64, I64, I64, I64, ctypes.POINTER(I64), ctypes.POINTER(I32), ctypes.POINTER(I32),
+        I64, I64, I64, I64, I32, ctypes.POINTER(I64), ctypes.POINTER(I32), ctypes.POINTER(I32),
         ctypes.POINTER(I64)]
     handle.kda_validate_metadata.argtypes = [P, P, I64, I64, I64, I64, ctypes.POINTER(I64)]
     handle.kda_epilogue_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, C, P, P]
@@ -132,11 +132,12 @@ def check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states
         num_seqs, activation, _ptr(out))
 
 
-def launch_shape(tokens: int, dim: int, part_dim: int, num_seqs: int) -> dict:
-    """The launch the library makes for these sizes (host only)."""
+def launch_shape(tokens: int, dim: int, part_dim: int, num_seqs: int, sm_count: int = 152) -> dict:
+    """The launch the library makes for these sizes on a GPU with `sm_count` SMs
+    (0: ask the current device)."""
     ctas, programs = ctypes.c_int64(), ctypes.c_int64()
     threads, chunk = ctypes.c_int32(), ctypes.c_int32()
-    _check(lib().kda_packed_conv1d_launch_shape(tokens, dim, part_dim, num_seqs,
+    _check(lib().kda_packed_conv1d_launch_shape(tokens, dim, part_dim, num_seqs, sm_count,
                                                 ctypes.byref(ctas), ctypes.byref(threads),
                                                 ctypes.byref(chunk), ctypes.byref(programs)))
     return {"ctas": ctas.value, "threads": threads.value, "chunk": chunk.value,

@@ -33,7 +33,43 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "kda_conv.h"
+
+// Launch geometry (compile-time; the defaults are the measured choice on GB300).
+#ifndef KDA_VEC
+#define KDA_VEC 4  // channels per thread: one 8-byte bf16 vector
+#endif
+#ifndef KDA_QUEUE
+#define KDA_QUEUE 9  // rows in flight per thread (a multiple of 3 keeps the history in place)
+#endif
+#ifndef KDA_CTA_THREADS
+#define KDA_CTA_THREADS 128
+#endif
+#ifndef KDA_MIN_BLOCKS
+#define KDA_MIN_BLOCKS 6  // resident CTAs per SM the register budget is sized for
+#endif
+#ifndef KDA_WAVES
+#define KDA_WAVES 1  // waves of resident warps a long prefill is spread over
+#endif
+#ifndef KDA_LOAD_L2_256
+#define KDA_LOAD_L2_256 0  // 1: x loads carry the L2::256B prefetch-size hint
+#endif
+#ifndef KDA_STORE_CS
+#define KDA_STORE_CS 0  // 1: plane stores use the streaming (evict-first) cache hint
+#endif
+
+#if KDA_LOAD_L2_256
+#define KDA_LD_X "ld.global.nc.L1::no_allocate.L2::256B"
+#else
+#define KDA_LD_X "ld.global.nc.L1::no_allocate"
+#endif
+#if KDA_STORE_CS
+#define KDA_ST_OUT "st.global.cs"
+#else
+#define KDA_ST_OUT "st.global"
+#endif
 
 namespace {
 
@@ -54,7 +90,8 @@ struct Params {
     void *out;
     int64_t plane_stride;  // tokens * part_dim elements
     int chunk;             // tokens per program (>= 4)
-    int col_blocks;        // channel blocks per token program
+    int warps_per_prog;    // warps covering one program's channel vectors
+    int64_t total_warps;   // programs * warps_per_prog
     int search_steps;      // radix-32 levels: smallest s with 32^s >= num_seqs
     int search_top;        // 32^(search_steps - 1)
 };
@@ -68,12 +105,12 @@ struct Params {
 template <int VEC>
 __device__ __forceinline__ void load_row(const uint16_t *p, uint32_t (&w)[VEC / 2]) {
     if constexpr (VEC == 8) {
-        asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        asm(KDA_LD_X ".v4.u32 {%0, %1, %2, %3}, [%4];"
             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
             : "l"(p));
     } else {
         static_assert(VEC == 4, "VEC must be 4 or 8");
-        asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+        asm(KDA_LD_X ".v2.u32 {%0, %1}, [%2];"
             : "=r"(w[0]), "=r"(w[1])
             : "l"(p));
     }
@@ -103,8 +140,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return u;
 }
 
-// SiLU in FP32: a / (1 + exp(-a)), IEEE division.
-__device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + expf(-a)); }
+// 2^x and 1/x on the special-function unit (PTX ex2.approx.ftz / rcp.approx.ftz:
+// relative error about 2^-22; subnormal inputs and results are flushed to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// SiLU in FP32: a / (1 + e^-a) with e^-a = 2^(-a log2 e), no branch.
+//   r = 1 / (0.25 (1 + e)) keeps the reciprocal's input below 2^126 for every
+//   finite e (e < 2^128), so r stays a normal number; y = a * (r * 0.25).
+// Where e^-a overflows (a <= -88.7228, the threshold of an IEEE expf) r is 0
+// and y is -0, as in the IEEE formula; a = -inf gives NaN, also as there.
+// Relative error about 2^-21 elsewhere, far inside half a bf16 ulp (2^-9):
+// after rounding, within one bf16 ulp of the IEEE formula (checked over all
+// 2^32 inputs).
+__device__ __forceinline__ float silu_f32(float a) {
+    const float e = ex2_approx(a * -1.44269504088896341f);
+    const float r = rcp_approx(__fmaf_rn(e, 0.25f, 0.25f));
+    return a * (r * 0.25f);
+}
+
+template <int VEC>
+__device__ __forceinline__ void silu_row(float (&y)[VEC]) {
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) y[v] = silu_f32(y[v]);
+}
 
 template <int VEC>
 __device__ __forceinline__ void store_bf16_row(uint16_t *p, const float (&y)[VEC]) {
@@ -112,11 +179,11 @@ __device__ __forceinline__ void store_bf16_row(uint16_t *p, const float (&y)[VEC
 #pragma unroll
     for (int i = 0; i < VEC / 2; ++i) w[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
     if constexpr (VEC == 8) {
-        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+        asm volatile(KDA_ST_OUT ".v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                      "r"(w[2]), "r"(w[3])
                      : "memory");
     } else {
-        asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
+        asm volatile(KDA_ST_OUT ".v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
                      : "memory");
     }
 }
@@ -151,11 +218,14 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
 // The conv kernel
 // ---------------------------------------------------------------------------
 
-template <int VEC, int U, bool kPreact, bool kSilu, bool kBias>
-__global__ void __launch_bounds__(256) kda_packed_conv1d_kernel(const Params p) {
+template <int VEC, int P, bool kPreact, bool kSilu, bool kBias>
+__global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
+    kda_packed_conv1d_kernel(const Params p) {
     const int lane = threadIdx.x & 31;
-    const int prog = blockIdx.x / p.col_blocks;
-    const int cb = blockIdx.x - prog * p.col_blocks;
+    const int64_t gwarp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (gwarp >= p.total_warps) return;  // whole warps only
+    const int prog = (int)(gwarp / p.warps_per_prog);
+    const int wv = (int)(gwarp - (int64_t)prog * p.warps_per_prog);
 
     const int s = find_sequence(p, prog, lane);
     if (s < 0) return;
@@ -172,7 +242,7 @@ __global__ void __launch_bounds__(256) kda_packed_conv1d_kernel(const Params p) 
     const int t0 = (int)t0_wide;
     const int t1 = min(t0 + p.chunk, e);
 
-    const int c = (cb * (int)blockDim.x + (int)threadIdx.x) * VEC;
+    const int c = (wv * 32 + lane) * VEC;
     if (c >= p.dim) return;
 
     // Taps and bias of this thread's channels.
@@ -198,6 +268,17 @@ __global__ void __launch_bounds__(256) kda_packed_conv1d_kernel(const Params p) 
 
     const uint16_t *xcol = p.x + c;
     const int64_t xs = p.x_row_stride;
+
+    // Register queue: slot u holds row t+u; it is refilled with row t+P+u as
+    // soon as row t+u has been widened, so P rows are always in flight.
+    uint32_t q[P][VEC / 2];
+#pragma unroll
+    for (int u = 0; u < P; ++u) {
+        if (t0 + u < t1)
+            load_row<VEC>(xcol + (int64_t)(t0 + u) * xs, q[u]);
+        else
+            zero_row<VEC>(q[u]);
+    }
 
     // History rows -3, -2, -1 relative to t0 (h0 oldest), in FP32.
     float h0[VEC], h1[VEC], h2[VEC];
@@ -264,31 +345,20 @@ __global__ void __launch_bounds__(256) kda_packed_conv1d_kernel(const Params p) 
 
     const int plane = c / p.part_dim;
     const int col = c - plane * p.part_dim;
-    const int64_t out_base = (int64_t)plane * p.plane_stride + col;
+    const int64_t out_row = p.part_dim;
+    int64_t o = (int64_t)plane * p.plane_stride + col + (int64_t)t0 * out_row;
+    const uint16_t *xnext = xcol + (int64_t)(t0 + P) * xs;
 
-    // Register queue: rows t .. t+U-1 are in `cur` while rows t+U .. t+2U-1 load.
-    uint32_t cur[U][VEC / 2];
+    // P rows per step.  Steps whose rows and refills all lie inside the chunk
+    // run without per-row bounds checks; the last one or two steps check.
+    int t = t0;
+    auto rows = [&](auto checked_tag) {
+        constexpr bool kChecked = decltype(checked_tag)::value;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        if (t0 + u < t1)
-            load_row<VEC>(xcol + (int64_t)(t0 + u) * xs, cur[u]);
-        else
-            zero_row<VEC>(cur[u]);
-    }
-    for (int t = t0; t < t1; t += U) {
-        uint32_t nxt[U][VEC / 2];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int r = t + U + u;
-            if (r < t1)
-                load_row<VEC>(xcol + (int64_t)r * xs, nxt[u]);
-            else
-                zero_row<VEC>(nxt[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
+        for (int u = 0; u < P; ++u) {
             float xv[VEC];
-            widen<VEC>(cur[u], xv);
+            widen<VEC>(q[u], xv);
+            if (!kChecked || t + P + u < t1) load_row<VEC>(xnext + (int64_t)u * xs, q[u]);
             float y[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
@@ -297,46 +367,48 @@ __global__ void __launch_bounds__(256) kda_packed_conv1d_kernel(const Params p) 
                 acc = __fmaf_rn(h1[v], w[v][1], acc);
                 acc = __fmaf_rn(h2[v], w[v][2], acc);
                 acc = __fmaf_rn(xv[v], w[v][3], acc);
-                y[v] = kSilu ? silu_f32(acc) : acc;
+                y[v] = acc;
                 h0[v] = h1[v];
                 h1[v] = h2[v];
                 h2[v] = xv[v];
             }
-            if (t + u < t1) {
-                const int64_t o = out_base + (int64_t)(t + u) * p.part_dim;
+            if constexpr (kSilu) silu_row<VEC>(y);
+            if (!kChecked || t + u < t1) {
                 if constexpr (kPreact)
-                    store_f32_row<VEC>(static_cast<float *>(p.out) + o, y);
+                    store_f32_row<VEC>(static_cast<float *>(p.out) + o + u * out_row, y);
                 else
-                    store_bf16_row<VEC>(static_cast<uint16_t *>(p.out) + o, y);
+                    store_bf16_row<VEC>(static_cast<uint16_t *>(p.out) + o + u * out_row, y);
             }
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-            for (int i = 0; i < VEC / 2; ++i) cur[u][i] = nxt[u][i];
-        }
-    }
+        xnext += P * xs;
+        o += P * out_row;
+    };
+    for (; t + 2 * P <= t1; t += P) rows(std::false_type{});
+    for (; t < t1; t += P) rows(std::true_type{});
 }
 
-// The epilogue alone, over consecutive fp32 bit patterns (two per thread step,
-// through the same pack as the conv kernel).
-template <bool kSilu>
+// The epilogue alone, over consecutive fp32 bit patterns, VEC at a time
+// through the same row functions as the conv kernel.  mode 0: rounding only;
+// 1: SiLU, then rounding.
+template <int VEC, int kMode>
 __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first, uint64_t count,
                                                                  uint16_t *out) {
-    const uint64_t step = 2ull * gridDim.x * blockDim.x;
-    for (uint64_t i = 2ull * (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x); i < count;
-         i += step) {
-        float lo = __uint_as_float(first + (uint32_t)i);
-        float hi = __uint_as_float(first + (uint32_t)(i + 1));
-        if (kSilu) {
-            lo = silu_f32(lo);
-            hi = silu_f32(hi);
+    const uint64_t step = (uint64_t)VEC * gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)VEC * (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x);
+         i < count; i += step) {
+        float y[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) y[v] = __uint_as_float(first + (uint32_t)(i + v));
+        if constexpr (kMode == 1) silu_row<VEC>(y);
+        if (i + VEC <= count) {
+            store_bf16_row<VEC>(out + i, y);
+        } else {
+            for (int v = 0; v < VEC && i + v < count; v += 2) {
+                const uint32_t wd = pack_bf16x2(y[v], y[v + 1]);
+                out[i + v] = (uint16_t)(wd & 0xFFFFu);
+                if (i + v + 1 < count) out[i + v + 1] = (uint16_t)(wd >> 16);
+            }
         }
-        const uint32_t w = pack_bf16x2(lo, hi);
-        if (i + 1 < count)
-            *reinterpret_cast<uint32_t *>(out + i) = w;
-        else
-            out[i] = (uint16_t)(w & 0xFFFFu);
     }
 }
 
@@ -346,10 +418,13 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 
 thread_local char g_last_error[256] = "";
 
-constexpr int kVec = 8;
-constexpr int kUnroll = 8;
-constexpr int kThreads = 128;
-constexpr int kChunk = 64;
+constexpr int kVec = KDA_VEC;                 // channels per thread
+constexpr int kQueue = KDA_QUEUE;             // rows in flight per thread
+constexpr int kThreads = KDA_CTA_THREADS;
+constexpr int kWarpsPerSm = KDA_CTA_THREADS / 32 * KDA_MIN_BLOCKS;
+constexpr int kDefaultSms = 152;              // GB300, for shape queries without a device
+constexpr int kMinChunk = 2 * KDA_QUEUE;
+constexpr int kMaxChunk = 2048;
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
@@ -386,23 +461,58 @@ struct Shape {
     int threads;
     int chunk;
     int64_t programs;
-    int col_blocks;
+    int warps_per_prog;
+    int64_t total_warps;
 };
 
-Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs) {
+// Chunk length.  The resident-warp budget is waves x SMs x warps per SM.
+// Preferred: the smallest multiple of the queue depth for which every program
+// (ceil(tokens/chunk) + num_seqs of them, the slack ones included) fits in the
+// budget at once, so no CTA waits for a later wave.  When num_seqs alone
+// exceeds the budget, the chunk that spreads the tokens over the budget.
+// Clamped to [kMinChunk, kMaxChunk].  It depends only on the scalar sizes and
+// the SM count, so a captured launch stays valid for new metadata.
+Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms) {
     Shape sh{};
     sh.threads = kThreads;
-    sh.chunk = kChunk;
+    const int64_t nvec = dim / kVec;
+    sh.warps_per_prog = (int)((nvec + 31) / 32);
+    const int64_t slots = (int64_t)KDA_WAVES * sms * kWarpsPerSm;
+    const int64_t max_programs = slots / sh.warps_per_prog;
+    int64_t chunk;
+    if (max_programs > num_seqs) {
+        chunk = (tokens + (max_programs - num_seqs) - 1) / (max_programs - num_seqs);
+    } else {
+        chunk = (tokens * sh.warps_per_prog + slots - 1) / slots;
+    }
+    chunk = (chunk + kQueue - 1) / kQueue * kQueue;
+    if (chunk < kMinChunk) chunk = kMinChunk;
+    if (chunk > kMaxChunk) chunk = kMaxChunk;
+    sh.chunk = (int)chunk;
     sh.programs = (tokens + sh.chunk - 1) / sh.chunk + num_seqs;
-    const int64_t per_block = (int64_t)kVec * sh.threads;
-    sh.col_blocks = (int)((dim + per_block - 1) / per_block);
-    sh.ctas = sh.programs * sh.col_blocks;
+    sh.total_warps = sh.programs * sh.warps_per_prog;
+    const int64_t warps_per_cta = kThreads / 32;
+    sh.ctas = (sh.total_warps + warps_per_cta - 1) / warps_per_cta;
     return sh;
+}
+
+// SM count of the current device, cached per device.
+int current_sms() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kDefaultSms;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = kDefaultSms;
+        cache[dev] = n;
+    }
+    return cache[dev];
 }
 
 template <bool kPreact, bool kSilu, bool kBias>
 void launch(const Params &p, const Shape &sh, cudaStream_t stream) {
-    kda_packed_conv1d_kernel<kVec, kUnroll, kPreact, kSilu, kBias>
+    kda_packed_conv1d_kernel<kVec, kQueue, kPreact, kSilu, kBias>
         <<<(unsigned)sh.ctas, sh.threads, 0, stream>>>(p);
 }
 
@@ -417,7 +527,7 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     if (st != KDA_OK) return st;
     if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;
 
-    const Shape sh = launch_shape(tokens, dim, num_seqs);
+    const Shape sh = launch_shape(tokens, dim, num_seqs, current_sms());
     if (sh.ctas > INT32_MAX) return KDA_ERR_INVALID_ARG;
     Params p;
     p.x = static_cast<const uint16_t *>(x);
@@ -436,7 +546,8 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.out = out;
     p.plane_stride = tokens * part_dim;
     p.chunk = sh.chunk;
-    p.col_blocks = sh.col_blocks;
+    p.warps_per_prog = sh.warps_per_prog;
+    p.total_warps = sh.total_warps;
     int steps = 0;
     int64_t reach = 1;
     while (reach < num_seqs) {
@@ -513,12 +624,15 @@ kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, i
 }
 
 kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t part_dim,
-                                            int64_t num_seqs, int64_t *ctas, int32_t *threads,
-                                            int32_t *chunk_tokens, int64_t *programs) {
+                                            int64_t num_seqs, int32_t sm_count, int64_t *ctas,
+                                            int32_t *threads, int32_t *chunk_tokens,
+                                            int64_t *programs) {
     kda_status_t st = check_sizes(dim, tokens, dim, part_dim, num_seqs);
     if (st != KDA_OK) return st;
     Shape sh{};
-    if (tokens > 0 && num_seqs > 0 && dim > 0) sh = launch_shape(tokens, dim, num_seqs);
+    if (sm_count < 0) return KDA_ERR_INVALID_ARG;
+    if (tokens > 0 && num_seqs > 0 && dim > 0)
+        sh = launch_shape(tokens, dim, num_seqs, sm_count > 0 ? sm_count : current_sms());
     if (ctas) *ctas = sh.ctas;
     if (threads) *threads = sh.threads;
     if (chunk_tokens) *chunk_tokens = sh.chunk;
@@ -575,16 +689,16 @@ kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, 
     if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
     if (count == 0) return KDA_OK;
     if (!out) return KDA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0) return KDA_ERR_MISALIGNED;
-    const uint64_t pairs = (count + 1) / 2;
+    if (!aligned16(out)) return KDA_ERR_MISALIGNED;
+    const uint64_t groups = (count + kVec - 1) / kVec;
     const unsigned threads = 256;
-    const uint64_t want = (pairs + threads - 1) / threads;
+    const uint64_t want = (groups + threads - 1) / threads;
     const unsigned blocks = (unsigned)(want < 152ull * 64 ? want : 152ull * 64);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (activation == KDA_ACT_SILU)
-        kda_epilogue_range_kernel<true><<<blocks, threads, 0, s>>>(first, count, out);
+        kda_epilogue_range_kernel<kVec, 1><<<blocks, threads, 0, s>>>(first, count, out);
     else
-        kda_epilogue_range_kernel<false><<<blocks, threads, 0, s>>>(first, count, out);
+        kda_epilogue_range_kernel<kVec, 0><<<blocks, threads, 0, s>>>(first, count, out);
     const cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) {
         snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
