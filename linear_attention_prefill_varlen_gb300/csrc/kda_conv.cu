@@ -42,13 +42,13 @@
 #define KDA_VEC 4  // channels per thread: one 8-byte bf16 vector
 #endif
 #ifndef KDA_QUEUE
-#define KDA_QUEUE 9  // rows in flight per thread (a multiple of 3 keeps the history in place)
+#define KDA_QUEUE 6  // rows in flight per thread (a multiple of 3 keeps the history in place)
 #endif
 #ifndef KDA_CTA_THREADS
 #define KDA_CTA_THREADS 128
 #endif
 #ifndef KDA_MIN_BLOCKS
-#define KDA_MIN_BLOCKS 6  // resident CTAs per SM the register budget is sized for
+#define KDA_MIN_BLOCKS 7  // resident CTAs per SM the register budget is sized for
 #endif
 #ifndef KDA_WAVES
 #define KDA_WAVES 1  // waves of resident warps a long prefill is spread over
@@ -57,7 +57,14 @@
 #define KDA_LOAD_L2_256 0  // 1: x loads carry the L2::256B prefetch-size hint
 #endif
 #ifndef KDA_STORE_CS
-#define KDA_STORE_CS 0  // 1: plane stores use the streaming (evict-first) cache hint
+#define KDA_STORE_CS 1  // 1: plane stores use the streaming (evict-first) cache hint
+#endif
+
+#ifndef KDA_LOAD_EVICT_FIRST
+#define KDA_LOAD_EVICT_FIRST 0  // 1: x loads carry an L2 evict-first cache policy
+#endif
+#ifndef KDA_STORE_EVICT_FIRST
+#define KDA_STORE_EVICT_FIRST 0  // 1: plane stores carry an L2 evict-first cache policy
 #endif
 
 #if KDA_LOAD_L2_256
@@ -104,16 +111,30 @@ struct Params {
 // low half of word i).  Streaming load: read once, keep out of L1.
 template <int VEC>
 __device__ __forceinline__ void load_row(const uint16_t *p, uint32_t (&w)[VEC / 2]) {
+    static_assert(VEC == 4 || VEC == 8, "VEC must be 4 or 8");
+#if KDA_LOAD_EVICT_FIRST
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    if constexpr (VEC == 8) {
+        asm(KDA_LD_X ".L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+            : "l"(p), "l"(pol));
+    } else {
+        asm(KDA_LD_X ".L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+            : "=r"(w[0]), "=r"(w[1])
+            : "l"(p), "l"(pol));
+    }
+#else
     if constexpr (VEC == 8) {
         asm(KDA_LD_X ".v4.u32 {%0, %1, %2, %3}, [%4];"
             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
             : "l"(p));
     } else {
-        static_assert(VEC == 4, "VEC must be 4 or 8");
         asm(KDA_LD_X ".v2.u32 {%0, %1}, [%2];"
             : "=r"(w[0]), "=r"(w[1])
             : "l"(p));
     }
+#endif
 }
 
 template <int VEC>
@@ -178,6 +199,19 @@ __device__ __forceinline__ void store_bf16_row(uint16_t *p, const float (&y)[VEC
     uint32_t w[VEC / 2];
 #pragma unroll
     for (int i = 0; i < VEC / 2; ++i) w[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
+#if KDA_STORE_EVICT_FIRST
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    if constexpr (VEC == 8) {
+        asm volatile(KDA_ST_OUT ".L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "l"(pol)
+                     : "memory");
+    } else {
+        asm volatile(KDA_ST_OUT ".L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(w[0]),
+                     "r"(w[1]), "l"(pol)
+                     : "memory");
+    }
+#else
     if constexpr (VEC == 8) {
         asm volatile(KDA_ST_OUT ".v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                      "r"(w[2]), "r"(w[3])
@@ -186,6 +220,7 @@ __device__ __forceinline__ void store_bf16_row(uint16_t *p, const float (&y)[VEC
         asm volatile(KDA_ST_OUT ".v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
                      : "memory");
     }
+#endif
 }
 
 template <int VEC>
