@@ -184,6 +184,15 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def aggregate(dist: Dist, world: int, nbytes_per_rank: int, region_ms: float, steps: int,
+              device) -> tuple[float, float]:
+    """Whole-job figures from one rank's timed region: the slowest rank's time
+    per step, and the bytes all ranks moved per second (GB/s)."""
+    slowest = dist.max(region_ms, device)
+    ms_per_step = slowest / steps
+    return ms_per_step, world * nbytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
     """Device copies of one batch.  dense_x stores x as (tokens, dim) contiguous."""
     x_np = b.x_buf[:, b.col_offset:b.col_offset + b.dim] if dense_x else b.x_buf
@@ -379,11 +388,9 @@ def run_ours(args) -> None:
     torch.cuda.synchronize(dev)
 
     t = time_device(pkg, b, sets, args.steps, args.warmup, dist, dev)
-    region_ms = dist.max(t["region_ms"], dev)
     kern_mean = statistics.fmean(t["kernel_ms"])
+    ms_per_step, value = aggregate(dist, world, nbytes, t["region_ms"], args.steps, dev)
     kern_mean_max = dist.max(kern_mean, dev)
-    ms_per_step = region_ms / args.steps
-    value = world * nbytes / (ms_per_step * 1e-3) / 1e9
 
     e2e = time_e2e(pkg, b, args.e2e_steps, dev)
     e2e_ms = dist.max(e2e["ms"], dev)
