@@ -69,6 +69,17 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_int, P, P, P,  # activation, out, preact, act
     ]
     lib.kda_ref_packed_conv1d.restype = ctypes.c_int
+    for name in ("kda_ref_f16_to_f32_n", "kda_ref_f16_rne_n"):
+        getattr(lib, name).argtypes = [P, I64, P]
+        getattr(lib, name).restype = None
+    lib.kda_ref_packed_conv1d_ex.argtypes = [
+        P, ctypes.c_int, I64, I64, I64, I64,  # x, dtype, x_row_stride, tokens, dim, part_dim
+        P, I64, I64, P,  # weight, w_stride_c, w_stride_j, bias
+        P, I64, I64, I64, I64, I64,  # conv_states, lines, width, strides (line, c, k)
+        P, P, P, I64, I64,  # cache_indices, has_initial_state, qsl, num_seqs, null_block_id
+        ctypes.c_int, P, P,  # activation, out, preact
+    ]
+    lib.kda_ref_packed_conv1d_ex.restype = ctypes.c_int
     return lib
 
 
@@ -185,4 +196,77 @@ def packed_conv1d(x_bits: np.ndarray, col_offset: int, dim: int, part_dim: int,
         res["preact"] = preact
     if want_act:
         res["act"] = act
+    return res
+
+
+DTYPE_BF16, DTYPE_F16, DTYPE_F32 = 0, 1, 2
+
+
+def f16_to_f32(bits: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Widens IEEE binary16 bit patterns (uint16) to fp32 via the oracle."""
+    lib = lib or load()
+    flat = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
+    out = np.empty(flat.size, dtype=np.float32)
+    lib.kda_ref_f16_to_f32_n(flat.ctypes.data, flat.size, out.ctypes.data)
+    return out.reshape(np.shape(bits))
+
+
+def f16_rne(values: np.ndarray, lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """Rounds fp32 values to binary16 bit patterns (uint16) via the oracle."""
+    lib = lib or load()
+    flat = np.ascontiguousarray(values, dtype=np.float32).ravel()
+    out = np.empty(flat.size, dtype=np.uint16)
+    lib.kda_ref_f16_rne_n(flat.ctypes.data, flat.size, out.ctypes.data)
+    return out.reshape(np.shape(values))
+
+
+def _elem_strides(a: np.ndarray) -> list[int]:
+    assert all(st % a.itemsize == 0 for st in a.strides)
+    return [st // a.itemsize for st in a.strides]
+
+
+def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, part_dim: int,
+                     weight: np.ndarray, bias: np.ndarray | None, conv_states: np.ndarray,
+                     cache_indices, has_initial_state, query_start_loc, null_block_id: int,
+                     activation: int, want_preact: bool = False,
+                     lib: ctypes.CDLL | None = None) -> dict:
+    """The general-layout oracle conv.
+
+    ``x_buf`` (tokens, row_stride): uint16 bits for bf16 / fp16, float32 for
+    fp32; the input is columns [col_offset, col_offset + dim).  ``weight`` is
+    a (dim, 4) float32 view with any strides; ``conv_states`` a
+    (lines, dim, K) float32 view with any strides, updated in place.  Returns
+    ``out`` (dim/part_dim, tokens, part_dim) of x's storage type, filled with
+    0xFFFF bits (NaN for fp32) where no sequence writes, and optionally
+    ``preact``."""
+    lib = lib or load()
+    assert x_buf.ndim == 2 and x_buf.flags["C_CONTIGUOUS"]
+    assert (x_buf.dtype == np.float32) == (dtype == DTYPE_F32)
+    tokens, row_stride = x_buf.shape
+    assert weight.dtype == np.float32 and weight.shape == (dim, 4)
+    assert conv_states.dtype == np.float32 and conv_states.ndim == 3
+    assert conv_states.shape[1] == dim
+    ws = _elem_strides(weight)
+    ss = _elem_strides(conv_states)
+    bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    ci = np.ascontiguousarray(cache_indices, dtype=np.int32)
+    his = np.ascontiguousarray(has_initial_state, dtype=np.uint8)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    planes = dim // part_dim
+    if dtype == DTYPE_F32:
+        out = np.full((planes, tokens, part_dim), np.nan, dtype=np.float32)
+    else:
+        out = np.full((planes, tokens, part_dim), 0xFFFF, dtype=np.uint16)
+    preact = np.full(out.shape, np.nan, dtype=np.float32) if want_preact else None
+    rc = lib.kda_ref_packed_conv1d_ex(
+        x_buf.ctypes.data + x_buf.itemsize * col_offset, dtype, row_stride, tokens, dim, part_dim,
+        weight.ctypes.data, ws[0], ws[1], _ptr(bias),
+        conv_states.ctypes.data, conv_states.shape[0], conv_states.shape[2], ss[0], ss[1], ss[2],
+        _ptr(ci), _ptr(his), _ptr(qsl), qsl.size - 1, null_block_id, activation,
+        out.ctypes.data, _ptr(preact))
+    if rc != REF_OK:
+        raise ValueError(f"oracle rejected the call: status {rc}")
+    res = {"out": out}
+    if want_preact:
+        res["preact"] = preact
     return res

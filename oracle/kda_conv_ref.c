@@ -221,3 +221,160 @@ int kda_ref_packed_conv1d(const uint16_t *x, int64_t x_row_stride, int64_t token
     }
     return REF_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* The general form: x / out in bf16, fp16 or fp32, a conv state of width     */
+/* K >= 3 with arbitrary element strides, and a strided weight.               */
+/* ------------------------------------------------------------------------ */
+
+#define REF_DTYPE_BF16 0
+#define REF_DTYPE_F16 1
+#define REF_DTYPE_F32 2
+
+/* IEEE binary16 -> fp32, exact, from the format's definition: 1 sign bit,
+ * 5 exponent bits (bias 15), 10 fraction bits; exponent 0 = zero/subnormal
+ * (value fraction * 2^-24), exponent 31 = infinity/NaN. */
+float kda_ref_f16_to_f32(uint16_t h) {
+    uint32_t sign = (uint32_t)(h >> 15) << 31;
+    uint32_t exp = (h >> 10) & 0x1Fu;
+    uint32_t frac = h & 0x3FFu;
+    if (exp == 0x1Fu) return f32_from_bits(sign | 0x7F800000u | (frac << 13));
+    if (exp != 0) return f32_from_bits(sign | ((exp + 112u) << 23) | (frac << 13));
+    /* zero or subnormal: frac * 2^-24, exact in fp32 */
+    float v = ldexpf((float)frac, -24);
+    return sign ? -v : v;
+}
+
+/* fp32 -> IEEE binary16, round to nearest, ties to even, from the definition:
+ * the result is the binary16 value nearest to f (the even one on a tie);
+ * values at or beyond 65520 (the largest finite half plus half an ulp) go to
+ * infinity.  NaN stays NaN with its sign (quiet bit set). */
+uint16_t kda_ref_f16_rne(float f) {
+    uint32_t u = bits_from_f32(f);
+    uint16_t sign = (uint16_t)((u >> 16) & 0x8000u);
+    uint32_t a = u & 0x7FFFFFFFu;
+    if (a > 0x7F800000u) return (uint16_t)(sign | 0x7E00u | ((a >> 13) & 0x3FFu));
+    if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u); /* >= 65520: inf */
+    int e = (int)(a >> 23) - 127;                               /* unbiased exponent */
+    uint32_t m = (a & 0x7FFFFFu) | (a >= 0x00800000u ? 0x800000u : 0u);
+    if (a < 0x00800000u) e = -126;                               /* fp32 subnormal */
+    /* the half quantum at this magnitude: 2^(e-10) for normal halves, 2^-24 below */
+    int q = (e >= -14) ? e - 10 : -24;
+    /* m * 2^(e-23) / 2^q = m >> (q - e + 23); round that shift to nearest even */
+    int shift = q - e + 23;
+    if (shift >= 32) return sign; /* far below the smallest subnormal half */
+    uint32_t kept = m >> shift;
+    uint32_t rem = m & ((1u << shift) - 1u);
+    uint32_t halfway = 1u << (shift - 1);
+    if (rem > halfway || (rem == halfway && (kept & 1u))) kept += 1u;
+    /* kept counts quanta of 2^q: for normal halves it includes the implicit
+     * 1024, and a carry to 2048 lands in the next binade */
+    if (q == -24) return (uint16_t)(sign | kept); /* subnormal (or the smallest normal) */
+    uint32_t biased = (uint32_t)(e + 15);
+    if (kept >= 2048u) {
+        kept >>= 1;
+        biased += 1u;
+    }
+    if (biased >= 31u) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (biased << 10) | (kept & 0x3FFu));
+}
+
+void kda_ref_f16_to_f32_n(const uint16_t *in, int64_t n, float *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kda_ref_f16_to_f32(in[i]);
+}
+
+void kda_ref_f16_rne_n(const float *in, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = kda_ref_f16_rne(in[i]);
+}
+
+static float ref_load(const void *x, int dtype, int64_t i) {
+    if (dtype == REF_DTYPE_BF16) return kda_ref_bf16_to_f32(((const uint16_t *)x)[i]);
+    if (dtype == REF_DTYPE_F16) return kda_ref_f16_to_f32(((const uint16_t *)x)[i]);
+    return ((const float *)x)[i];
+}
+
+static void ref_store(void *out, int dtype, int64_t i, float y) {
+    if (dtype == REF_DTYPE_BF16)
+        ((uint16_t *)out)[i] = kda_ref_bf16_rne(y);
+    else if (dtype == REF_DTYPE_F16)
+        ((uint16_t *)out)[i] = kda_ref_f16_rne(y);
+    else
+        ((float *)out)[i] = y;
+}
+
+/*
+ * The conv with the general layout.  Differences from kda_ref_packed_conv1d:
+ *   x and out are of type `dtype` (bf16, fp16 or fp32; out has x's type, as
+ *   packed_causal_conv1d_fn returns x.dtype); fp16 / bf16 outputs are rounded
+ *   to nearest even, fp32 outputs are the FP32 result itself;
+ *   weight[c][j] is at weight[c * w_stride_c + j * w_stride_j];
+ *   the conv state of a line holds the K = state_width most recent rows,
+ *   position K-1 the newest, element (line, c, k) at
+ *   conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k].
+ *   The taps read its last 3 positions; afterwards the line holds the last K
+ *   rows of [old state (or zeros) ; the sequence's rows].
+ * With dtype bf16, K = 3 and contiguous strides this is kda_ref_packed_conv1d.
+ */
+int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int64_t tokens,
+                             int64_t dim, int64_t part_dim, const float *weight,
+                             int64_t w_stride_c, int64_t w_stride_j, const float *bias,
+                             float *conv_states, int64_t cache_lines, int64_t state_width,
+                             int64_t s_stride_line, int64_t s_stride_c, int64_t s_stride_k,
+                             const int32_t *cache_indices, const uint8_t *has_initial_state,
+                             const int32_t *query_start_loc, int64_t num_seqs,
+                             int64_t null_block_id, int activation, void *out, float *preact) {
+    int64_t bad;
+    if (tokens < 0 || dim < 0 || part_dim <= 0 || num_seqs < 0) return REF_BAD_SHAPE;
+    if (dim % part_dim != 0 || x_row_stride < dim) return REF_BAD_SHAPE;
+    if (activation != 0 && activation != 1) return REF_BAD_SHAPE;
+    if (dtype != REF_DTYPE_BF16 && dtype != REF_DTYPE_F16 && dtype != REF_DTYPE_F32)
+        return REF_BAD_SHAPE;
+    if (state_width < 3 || state_width > 64) return REF_BAD_SHAPE;
+    if (tokens == 0 || num_seqs == 0) return REF_OK;
+    int rc = kda_ref_check_metadata(tokens, cache_lines, cache_indices, query_start_loc, num_seqs,
+                                    null_block_id, &bad);
+    if (rc != REF_OK) return rc;
+    const int64_t K = state_width;
+
+    for (int64_t s = 0; s < num_seqs; ++s) {
+        int64_t a = query_start_loc[s];
+        int64_t len = (int64_t)query_start_loc[s + 1] - a;
+        if (len <= 0) continue;
+        int64_t line = cache_indices[s];
+        int is_null = (line == null_block_id);
+        int read_state = (!is_null) && (has_initial_state[s] != 0);
+
+        for (int64_t c = 0; c < dim; ++c) {
+            float h[64];
+            for (int64_t k = 0; k < K; ++k)
+                h[k] = read_state ? conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k]
+                                  : 0.0f;
+            int64_t plane = c / part_dim;
+            int64_t col = c % part_dim;
+
+            for (int64_t t = 0; t < len; ++t) {
+                float acc = (bias != NULL) ? bias[c] : 0.0f;
+                for (int j = 0; j <= 3; ++j) {
+                    int64_t r = t - 3 + j;
+                    float v = (r >= 0) ? ref_load(x, dtype, (a + r) * x_row_stride + c) : h[K + r];
+                    acc = fmaf(v, weight[c * w_stride_c + j * w_stride_j], acc);
+                }
+                float y = activation ? kda_ref_silu(acc) : acc;
+                int64_t oi = (plane * tokens + (a + t)) * part_dim + col;
+                ref_store(out, dtype, oi, y);
+                if (preact) preact[oi] = acc;
+            }
+
+            if (!is_null) {
+                float ns[64];
+                for (int64_t k = 0; k < K; ++k) {
+                    int64_t r = len - K + k;
+                    ns[k] = (r >= 0) ? ref_load(x, dtype, (a + r) * x_row_stride + c) : h[k + len];
+                }
+                for (int64_t k = 0; k < K; ++k)
+                    conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k] = ns[k];
+            }
+        }
+    }
+    return REF_OK;
+}

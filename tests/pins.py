@@ -498,3 +498,195 @@ ALL_PINS = [
     pin_silu_and_rounding, pin_closed_forms, pin_chunk_carry, pin_zero_history,
     pin_short_state_shift, pin_permutation, pin_untouched, pin_metadata_checks,
 ]
+
+
+# --------------------------------------------------------------------------
+# The general-layout oracle: fp16 / fp32 x, state width K >= 3, strides
+# --------------------------------------------------------------------------
+
+def torch_f16_to_f32(bits: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(torch.float16).float().numpy()
+
+
+def torch_f32_to_f16(vals: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(vals, dtype=np.float32))
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
+def x_as_f32(b: workloads.Batch, rows) -> np.ndarray:
+    """Input columns of b for the given rows, widened by torch's conversions."""
+    xs = b.x_buf[rows, b.col_offset:b.col_offset + b.dim]
+    if b.x_dtype == "bf16":
+        return torch_bf16_to_f32(xs)
+    if b.x_dtype == "f16":
+        return torch_f16_to_f32(xs)
+    return np.asarray(xs, dtype=np.float32)
+
+
+DT = {"bf16": oracle.DTYPE_BF16, "f16": oracle.DTYPE_F16, "f32": oracle.DTYPE_F32}
+
+
+def run_oracle_ex(b: workloads.Batch, lib=None, weight=None, states=None, **kw) -> dict:
+    return oracle.packed_conv1d_ex(
+        b.x_buf, DT[b.x_dtype], b.col_offset, b.dim, b.part_dim,
+        b.weight if weight is None else weight, b.bias,
+        b.conv_states if states is None else states, b.cache_indices, b.has_initial_state,
+        b.query_start_loc, b.null_block_id, b.activation, lib=lib, **kw)
+
+
+def pin_f16_widen(lib) -> None:
+    """Every binary16 pattern widens to torch's value (NaN to NaN)."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got, want = oracle.f16_to_f32(allb, lib), torch_f16_to_f32(allb)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+F16_CASES = [  # (fp32 bits, binary16 bits) worked from round-half-even
+    (0x3F801000, 0x3C00),  # 1 + 2^-11: tie, even below
+    (0x3F803000, 0x3C02),  # 1 + 3*2^-11: tie, odd below -> up
+    (0x3F801001, 0x3C01),  # just above the tie
+    (0x477FE000, 0x7BFF),  # 65504, the largest finite half
+    (0x477FEFFF, 0x7BFF),  # just below 65520
+    (0x477FF000, 0x7C00),  # 65520: tie to the even neighbour 65536 = overflow
+    (0x33800000, 0x0001),  # 2^-24, the smallest subnormal half
+    (0x33000000, 0x0000),  # 2^-25: tie between 0 and 2^-24 -> 0
+    (0x33000001, 0x0001),  # just above that tie
+    (0x33C00000, 0x0002),  # 3 * 2^-25: tie between 1 and 2 quanta -> 2
+    (0x387FE000, 0x0400),  # 1023.5 * 2^-24: tie -> the smallest normal 2^-14
+    (0x387FC000, 0x03FF),  # 1023 * 2^-24, the largest subnormal half, exactly
+    (0x80000000, 0x8000),  # -0
+    (0x7F800000, 0x7C00),
+    (0xFF800000, 0xFC00),
+]
+
+
+def pin_f16_rne(lib, seed: int = 9) -> None:
+    """Hand-worked cases, every tie between neighbouring halves, dense samples
+    of the half range and random patterns, against torch's fp32 -> fp16."""
+    src = np.array([c[0] for c in F16_CASES], dtype=np.uint32).view(np.float32)
+    want = np.array([c[1] for c in F16_CASES], dtype=np.uint16)
+    got = oracle.f16_rne(src, lib)
+    assert np.array_equal(got, want), [hex(v) for v in got]
+    halves = torch_f16_to_f32(np.arange(0, 0x7C00, dtype=np.uint16)).astype(np.float64)
+    ties = ((halves[:-1] + halves[1:]) / 2).astype(np.float32)  # exact in fp32
+    rng = np.random.default_rng(seed)
+    dense = (2.0 ** rng.uniform(-27, 17, size=1 << 20)).astype(np.float32)
+    pats = rng.integers(0, 2 ** 32, size=1 << 20, dtype=np.uint64).astype(np.uint32)
+    for v in (ties, -ties, dense, -dense, pats.view(np.float32)):
+        nan = np.isnan(v)
+        g, w = oracle.f16_rne(v, lib), torch_f32_to_f16(v)
+        assert np.array_equal(g[~nan], w[~nan])
+        assert (((g[nan] & 0x7C00) == 0x7C00) & ((g[nan] & 0x3FF) != 0)).all()
+
+
+def pin_ex_matches_basic(lib) -> None:
+    """With bf16, width 3 and contiguous strides the general oracle computes
+    bit for bit what the first one does (both pinned independently)."""
+    for seed, lengths, act, bias in [(111, [5, 0, 70, 1, 2], 1, True), (112, [33, 3], 0, False)]:
+        b = small_batch(seed, lengths, dim=128, part_dim=64, null_count=1, activation=act,
+                        bias=bias, cache_lines=8)
+        s1, s2 = b.conv_states.copy(), b.conv_states.copy()
+        r1 = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, s1,
+                                  b.cache_indices, b.has_initial_state, b.query_start_loc,
+                                  b.null_block_id, act, lib=lib)
+        r2 = run_oracle_ex(b, lib, states=s2)
+        assert np.array_equal(r1["out"], r2["out"])
+        assert np.array_equal(s1.view(np.uint32), s2.view(np.uint32))
+
+
+def pin_ex_typed_exact(lib) -> None:
+    """fp16 and fp32 x: pre-activations bit-identical to the exact-rational
+    FMA chain over the padded column; outputs = torch's rounding of them."""
+    for x_dtype, seed in (("f16", 121), ("f32", 122)):
+        b = workloads.make_batch(f"t{seed}", seed, [4, 1, 6], 64, 64, 80, 5, col_offset=8,
+                                 activation=0, his_p=0.7, null_count=1, x_dtype=x_dtype)
+        st = b.conv_states.copy()
+        res = run_oracle_ex(b, lib, states=st, want_preact=True)
+        pre = plane_view(res["preact"], b)
+        w = b.weight.astype(np.float64)
+        for s in range(b.num_seqs):
+            a, e = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+            line = int(b.cache_indices[s])
+            hist = np.zeros((3, b.dim))
+            if line != b.null_block_id and b.has_initial_state[s]:
+                hist = b.conv_states[line].T.astype(np.float64)
+            col = np.concatenate([hist, x_as_f32(b, slice(a, e)).astype(np.float64)])
+            for t in range(e - a):
+                for c in range(b.dim):
+                    acc = float(np.float32(b.bias[c]))
+                    for j in range(4):
+                        acc = fma_f32(float(col[t + j, c]), float(w[c, j]), acc)
+                    assert np.float32(acc).view(np.uint32) == pre[a + t, c].view(np.uint32)
+        written = ~np.isnan(res["preact"])
+        if x_dtype == "f16":
+            assert np.array_equal(res["out"][written], torch_f32_to_f16(res["preact"][written]))
+        else:
+            assert np.array_equal(res["out"][written].view(np.uint32),
+                                  res["preact"][written].view(np.uint32))
+
+
+def pin_ex_state_width(lib) -> None:
+    """Width K > 3: the taps read the K-3 .. K-1 positions (same outputs as a
+    width-3 state holding them); afterwards the line holds the last K rows of
+    [old line or zeros ; the sequence's rows]; splitting a sequence over two
+    calls with the line carried equals one call."""
+    for K in (4, 7):
+        b = workloads.make_batch(f"k{K}", 130 + K, [1, 2, 5, 9, 20], 64, 64, 72, 8,
+                                 col_offset=8, his_p=0.6, null_count=1, state_width=K)
+        stK = b.conv_states.copy()
+        rK = run_oracle_ex(b, lib, states=stK)
+        b3 = b.copy()
+        b3.conv_states = np.ascontiguousarray(b.conv_states[:, :, K - 3:])
+        r3 = run_oracle_ex(b3, lib, states=b3.conv_states)
+        assert np.array_equal(rK["out"], r3["out"])
+        for s in range(b.num_seqs):
+            line = int(b.cache_indices[s])
+            if line == b.null_block_id:
+                continue
+            a, e = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+            old = b.conv_states[line] if b.has_initial_state[s] else np.zeros((b.dim, K), np.float32)
+            want = np.concatenate([old.T, x_as_f32(b, slice(a, e))])[-K:].T
+            assert np.array_equal(stK[line].view(np.uint32), want.view(np.uint32)), (K, s)
+    # chunk carry at width 5
+    K = 5
+    b = workloads.make_batch("carry5", 141, [30, 7, 2], 64, 64, 64, 4, his_p=0.5, state_width=K)
+    full_st = b.conv_states.copy()
+    full = plane_view(run_oracle_ex(b, lib, states=full_st)["out"], b)
+    qsl = b.query_start_loc
+    cut = [11, 3, 1]
+    first = [(int(qsl[s]), int(qsl[s]) + cut[s]) for s in range(3)]
+    second = [(int(qsl[s]) + cut[s], int(qsl[s + 1])) for s in range(3)]
+    c1 = _sub_batch(b, first, b.has_initial_state, b.conv_states.copy())
+    o1 = plane_view(run_oracle_ex(c1, lib, states=c1.conv_states)["out"], c1)
+    c2 = _sub_batch(b, second, np.ones(3), c1.conv_states)
+    o2 = plane_view(run_oracle_ex(c2, lib, states=c2.conv_states)["out"], c2)
+    assert np.array_equal(c2.conv_states.view(np.uint32), full_st.view(np.uint32))
+    r1 = r2 = 0
+    for s in range(3):
+        (a1, e1), (a2, e2) = first[s], second[s]
+        assert np.array_equal(o1[r1:r1 + e1 - a1], full[a1:e1])
+        assert np.array_equal(o2[r2:r2 + e2 - a2], full[a2:e2])
+        r1, r2 = r1 + e1 - a1, r2 + e2 - a2
+
+
+def pin_ex_strides(lib) -> None:
+    """The same call with the state stored position-major and the weight
+    tap-major (width-major) gives the same outputs and the same state values."""
+    K = 4
+    b = workloads.make_batch("strides", 151, [3, 12, 1], 128, 64, 136, 6, col_offset=8,
+                             his_p=0.7, null_count=1, state_width=K)
+    st = b.conv_states.copy()
+    ref = run_oracle_ex(b, lib, states=st)
+    mem_s = np.ascontiguousarray(b.conv_states.transpose(0, 2, 1))  # (lines, K, dim)
+    view_s = mem_s.transpose(0, 2, 1)  # (lines, dim, K) view, strides (K*dim, 1, dim)
+    mem_w = np.ascontiguousarray(b.weight.T)  # (4, dim): tap-major
+    got = run_oracle_ex(b, lib, weight=mem_w.T, states=view_s)
+    assert np.array_equal(got["out"], ref["out"])
+    assert np.array_equal(np.ascontiguousarray(view_s).view(np.uint32), st.view(np.uint32))
+
+
+ALL_PINS += [pin_f16_widen, pin_f16_rne, pin_ex_matches_basic, pin_ex_typed_exact,
+             pin_ex_state_width, pin_ex_strides]

@@ -38,6 +38,16 @@ MUTANTS = [
      "int64_t o = (a + t) * dim + c;"),
     ("widen_shift", "return f32_from_bits((uint32_t)h << 16);",
      "return f32_from_bits(((uint32_t)h << 16) | 1u);"),
+    # the general-layout function and the binary16 conversions
+    ("ex_taps_first3", ": h[K + r];", ": h[3 + r];"),
+    ("ex_state_not_shifted", ": h[k + len];", ": h[k];"),
+    ("ex_weight_stride_ignored", "acc = fmaf(v, weight[c * w_stride_c + j * w_stride_j], acc);",
+     "acc = fmaf(v, weight[c * 4 + j], acc);"),
+    ("f16_ties_away", "if (rem > halfway || (rem == halfway && (kept & 1u))) kept += 1u;",
+     "if (rem >= halfway) kept += 1u;"),
+    ("f16_no_subnormals", "int q = (e >= -14) ? e - 10 : -24;", "int q = e - 10;"),
+    ("f16_widen_subnormal", "float v = ldexpf((float)frac, -24);",
+     "float v = ldexpf((float)frac, -25);"),
 ]
 
 

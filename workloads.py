@@ -53,6 +53,7 @@ class Batch:
     activation: int  # 0 none, 1 SiLU
     seed: int
     notes: dict = field(default_factory=dict)
+    x_dtype: str = "bf16"  # storage of x and out: "bf16" / "f16" (uint16 bits) or "f32"
 
     @property
     def tokens(self) -> int:
@@ -77,18 +78,29 @@ class Batch:
             self.weight.copy(), None if self.bias is None else self.bias.copy(),
             self.conv_states.copy(), self.cache_indices.copy(), self.has_initial_state.copy(),
             self.query_start_loc.copy(), self.null_block_id, self.activation, self.seed,
-            dict(self.notes))
+            dict(self.notes), self.x_dtype)
 
 
 def _bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def _x_storage(t: torch.Tensor, x_dtype: str) -> np.ndarray:
+    """fp32 samples stored as the call's x type, by torch's own conversion."""
+    if x_dtype == "bf16":
+        return _bf16_bits(t)
+    if x_dtype == "f16":
+        return t.to(torch.float16).contiguous().view(torch.int16).numpy().view(np.uint16)
+    assert x_dtype == "f32"
+    return t.contiguous().numpy().astype(np.float32)
+
+
 def make_batch(name: str, seed: int, lengths, dim: int, part_dim: int, row_stride: int,
                cache_lines: int, *, col_offset: int = 0, x_std: float = 1.0,
                w_range: float = 0.5, bias_std: float | None = 0.1, activation: int = 1,
                his_p: float = 1.0, his: list[int] | None = None, null_count: int = 0,
-               tokens: int | None = None, first_token: int = 0) -> Batch:
+               tokens: int | None = None, first_token: int = 0, x_dtype: str = "bf16",
+               state_width: int = 3) -> Batch:
     """Draws one batch.
 
     Draw order: lengths are given; x (tokens, row_stride) ~ N(0, x_std^2);
@@ -110,12 +122,12 @@ def make_batch(name: str, seed: int, lengths, dim: int, part_dim: int, row_strid
     qsl[1:] = first_token + np.cumsum(np.asarray(lengths, dtype=np.int64))
     total = int(qsl[-1]) if tokens is None else int(tokens)
     assert total >= int(qsl[-1])
-    x = _bf16_bits(torch.randn(total, row_stride, generator=g) * x_std)
+    x = _x_storage(torch.randn(total, row_stride, generator=g) * x_std, x_dtype)
     w = ((torch.rand(dim, 4, generator=g) * 2.0 - 1.0) * w_range).numpy().astype(np.float32)
     b = None
     if bias_std is not None:
         b = (torch.randn(dim, generator=g) * bias_std).numpy().astype(np.float32)
-    s = torch.randn(cache_lines, dim, 3, generator=g).numpy().astype(np.float32)
+    s = torch.randn(cache_lines, dim, state_width, generator=g).numpy().astype(np.float32)
     assert n <= cache_lines
     ci = torch.randperm(cache_lines, generator=g)[:n].numpy().astype(np.int32)
     if his is None:
@@ -126,7 +138,8 @@ def make_batch(name: str, seed: int, lengths, dim: int, part_dim: int, row_strid
         pos = torch.randperm(n, generator=g)[:null_count].numpy()
         ci[pos] = NULL_BLOCK_ID
     return Batch(name, np.ascontiguousarray(x), col_offset, dim, part_dim, np.ascontiguousarray(w),
-                 b, np.ascontiguousarray(s), ci, hv, qsl, NULL_BLOCK_ID, activation, seed)
+                 b, np.ascontiguousarray(s), ci, hv, qsl, NULL_BLOCK_ID, activation, seed,
+                 x_dtype=x_dtype)
 
 
 def _lengths(seed: int, n: int, lo: int, hi: int) -> list[int]:
@@ -181,5 +194,7 @@ def algorithmic_bytes(b: Batch) -> int:
     reads = int(np.count_nonzero(live & not_null & (b.has_initial_state != 0)))
     writes = int(np.count_nonzero(live & not_null))
     d = b.dim
-    return (2 * rows * d + 2 * rows * d + 12 * d * reads + 12 * d * writes + 16 * d
+    xb = 4 if b.x_dtype == "f32" else 2
+    sb = 4 * b.conv_states.shape[2]
+    return (2 * xb * rows * d + sb * d * reads + sb * d * writes + 16 * d
             + (4 * d if b.bias is not None else 0))
