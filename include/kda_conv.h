@@ -62,6 +62,30 @@ typedef enum {
 
 typedef enum { KDA_ACT_NONE = 0, KDA_ACT_SILU = 1 } kda_activation_t;
 
+/* Storage type of x and out (kda_packed_conv1d_ex). */
+typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F16 = 1, KDA_DTYPE_F32 = 2 } kda_dtype_t;
+
+/*
+ * The general layout of kda_packed_conv1d_ex, after packed_causal_conv1d_supported
+ * on the kda_conv page: x may be bf16, fp16 or fp32 (out has x's type, as
+ * packed_causal_conv1d_fn returns x.dtype), the FP32 weight and conv state are
+ * passed with their strides, and the conv state may be wider than 3.
+ *   x_dtype        kda_dtype_t of x and out.
+ *   state_width    K = conv_states size(2), 3..64. A line holds the K most recent
+ *                  rows (position K-1 the newest); the taps read positions K-3..K-1;
+ *                  afterwards the line holds the last K rows of [old line (or zeros
+ *                  without an initial state) ; the sequence's rows].
+ *   state_stride   element strides of conv_states: line, channel, position.
+ *   weight_stride  element strides of weight: channel, tap (4, 1 is channel-major;
+ *                  1, dim is the tap-major layout of a width-major weight copy).
+ */
+typedef struct kda_conv_layout {
+    int32_t x_dtype;
+    int32_t state_width;
+    int64_t state_stride[3];
+    int64_t weight_stride[2];
+} kda_conv_layout_t;
+
 /*
  * kda_packed_conv1d -- the conv, one launch.
  *
@@ -103,6 +127,23 @@ kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t toke
                                kda_stream_t stream);
 
 /*
+ * kda_packed_conv1d_ex -- kda_packed_conv1d with the general layout above; layout
+ * NULL means bf16, width 3 and contiguous strides (kda_packed_conv1d itself).
+ * Rounding of out: bf16 and fp16 to nearest even, fp32 none. Alignment: x and out
+ * 16-byte aligned and x_row_stride a multiple of 16 bytes (8 elements of bf16 /
+ * fp16, 4 of fp32); weight 16-byte aligned when its strides are (4, 1), else
+ * 4-byte; conv_states 16-byte aligned when it is width 3 and contiguous, else
+ * 4-byte; bias 16-byte aligned. Everything else as for kda_packed_conv1d.
+ */
+kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t tokens,
+                                  int64_t dim, int64_t part_dim, const float *weight,
+                                  const float *bias, float *conv_states,
+                                  const int32_t *cache_indices, const uint8_t *has_initial_state,
+                                  const int32_t *query_start_loc, int64_t num_seqs,
+                                  int64_t null_block_id, int activation, void *out,
+                                  const kda_conv_layout_t *layout, kda_stream_t stream);
+
+/*
  * kda_packed_conv1d_preact_f32 -- the same conv without activation or rounding:
  * `out` receives the FP32 accumulator (dim/part_dim, tokens, part_dim) and the conv
  * state is updated exactly as by kda_packed_conv1d. Same arguments and rules as
@@ -129,6 +170,15 @@ kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, i
                                           const uint8_t *has_initial_state,
                                           const int32_t *query_start_loc, int64_t num_seqs,
                                           int activation, const void *out);
+
+/* kda_packed_conv1d_ex_check_args -- host only: the argument check of
+ * kda_packed_conv1d_ex (as kda_packed_conv1d_check_args, with a layout). */
+kda_status_t kda_packed_conv1d_ex_check_args(
+    const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
+    const float *weight, const float *bias, const float *conv_states,
+    const int32_t *cache_indices, const uint8_t *has_initial_state,
+    const int32_t *query_start_loc, int64_t num_seqs, int activation, const void *out,
+    const kda_conv_layout_t *layout);
 
 /*
  * kda_packed_conv1d_launch_shape -- the launch kda_packed_conv1d makes for these

@@ -16,11 +16,18 @@ from __future__ import annotations
 from ._binding import (  # noqa: F401
     KDA_ACT_NONE,
     KDA_ACT_SILU,
+    KDA_DTYPE_BF16,
+    KDA_DTYPE_F16,
+    KDA_DTYPE_F32,
     KDA_OK,
+    KdaConvLayout,
     KdaError,
     epilogue_range,
     kda_packed_conv1d,
+    kda_packed_conv1d_ex,
     kda_packed_conv1d_preact_f32,
+    layout_of,
+    make_layout,
     launch_shape,
     lib,
     lib_path,

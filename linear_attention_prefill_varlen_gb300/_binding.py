@@ -18,6 +18,9 @@ KDA_ERR_CUDA = 4
 KDA_ERR_METADATA = 5
 KDA_ACT_NONE = 0
 KDA_ACT_SILU = 1
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_F16 = 1
+KDA_DTYPE_F32 = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -31,6 +34,18 @@ class KdaError(RuntimeError):
         super().__init__(what)
 
 
+class KdaConvLayout(ctypes.Structure):
+    """kda_conv_layout_t: x/out dtype, conv-state width and element strides."""
+
+    _fields_ = [("x_dtype", ctypes.c_int32), ("state_width", ctypes.c_int32),
+                ("state_stride", ctypes.c_int64 * 3), ("weight_stride", ctypes.c_int64 * 2)]
+
+
+def make_layout(x_dtype: int, state_width: int, state_stride, weight_stride) -> KdaConvLayout:
+    return KdaConvLayout(x_dtype, state_width, (ctypes.c_int64 * 3)(*state_stride),
+                         (ctypes.c_int64 * 2)(*weight_stride))
+
+
 def lib_path() -> str:
     return _build.LIB_PATH
 
@@ -40,6 +55,9 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     conv = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64, I64]
     handle.kda_packed_conv1d.argtypes = conv + [C, P, P]
     handle.kda_packed_conv1d_preact_f32.argtypes = conv + [P, P]
+    handle.kda_packed_conv1d_ex.argtypes = conv + [C, P, ctypes.POINTER(KdaConvLayout), P]
+    handle.kda_packed_conv1d_ex_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P,
+                                                       I64, C, P, ctypes.POINTER(KdaConvLayout)]
     handle.kda_packed_conv1d_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64,
                                                     C, P]
     handle.kda_packed_conv1d_launch_shape.argtypes = [
@@ -47,7 +65,8 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.POINTER(I64)]
     handle.kda_validate_metadata.argtypes = [P, P, I64, I64, I64, I64, ctypes.POINTER(I64)]
     handle.kda_epilogue_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, C, P, P]
-    for name in ("kda_packed_conv1d", "kda_packed_conv1d_preact_f32",
+    for name in ("kda_packed_conv1d", "kda_packed_conv1d_preact_f32", "kda_packed_conv1d_ex",
+                 "kda_packed_conv1d_ex_check_args",
                  "kda_packed_conv1d_check_args", "kda_packed_conv1d_launch_shape",
                  "kda_validate_metadata", "kda_epilogue_range"):
         getattr(handle, name).restype = C
@@ -111,6 +130,28 @@ def kda_packed_conv1d(x, x_row_stride: int, tokens: int, dim: int, part_dim: int
         num_seqs, null_block_id, activation, _ptr(out), _stream(stream)))
 
 
+def kda_packed_conv1d_ex(x, x_row_stride: int, tokens: int, dim: int, part_dim: int, weight,
+                         bias, conv_states, cache_indices, has_initial_state, query_start_loc,
+                         num_seqs: int, null_block_id: int, activation: int, out,
+                         layout: KdaConvLayout | None, stream=None) -> None:
+    """C-ABI kda_packed_conv1d_ex (layout None: the default layout)."""
+    _check(lib().kda_packed_conv1d_ex(
+        _ptr(x), x_row_stride, tokens, dim, part_dim, _ptr(weight), _ptr(bias),
+        _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
+        num_seqs, null_block_id, activation, _ptr(out),
+        None if layout is None else ctypes.byref(layout), _stream(stream)))
+
+
+def check_args_ex(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
+                  cache_indices, has_initial_state, query_start_loc, num_seqs, activation, out,
+                  layout: KdaConvLayout | None) -> int:
+    """Host-only argument check of kda_packed_conv1d_ex; returns the status."""
+    return lib().kda_packed_conv1d_ex_check_args(
+        _ptr(x), x_row_stride, tokens, dim, part_dim, _ptr(weight), _ptr(bias),
+        _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
+        num_seqs, activation, _ptr(out), None if layout is None else ctypes.byref(layout))
+
+
 def kda_packed_conv1d_preact_f32(x, x_row_stride: int, tokens: int, dim: int, part_dim: int,
                                  weight, bias, conv_states, cache_indices, has_initial_state,
                                  query_start_loc, num_seqs: int, null_block_id: int, out,
@@ -162,25 +203,34 @@ def epilogue_range(first: int, count: int, activation: int, out, stream=None) ->
 
 
 _SILU_NAMES = ("silu", "swish", True)
+_DTYPES = {torch.bfloat16: KDA_DTYPE_BF16, torch.float16: KDA_DTYPE_F16,
+           torch.float32: KDA_DTYPE_F32}
 
 
 def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
                                    conv_states: torch.Tensor, part_dim: int) -> bool:
-    """Whether packed_causal_conv1d_fn takes these inputs on this library: bf16 x
-    on CUDA with unit channel stride and 16-byte aligned rows, FP32 weight
-    (dim, 4) and contiguous FP32 conv_states (lines, dim, 3), part_dim a
-    multiple of 64 dividing dim (the page's predicate narrowed to what the
-    kernel reads)."""
+    """Whether packed_causal_conv1d_fn takes these inputs: the page's predicate
+    (x CUDA, 2-D, unit channel stride, bf16 / fp16 / fp32; FP32 weight (dim, 4)
+    and conv_states (lines, dim, >= 3), any strides; part_dim a multiple of 64
+    dividing dim) plus this library's alignment rules (x rows on 16-byte
+    boundaries, state width at most 64)."""
+    if not (x.is_cuda and x.dim() == 2 and x.stride(1) == 1 and x.dtype in _DTYPES):
+        return False
+    quantum = 4 if x.dtype == torch.float32 else 8
     return (
-        x.is_cuda and x.dim() == 2 and x.stride(1) == 1 and x.dtype == torch.bfloat16
-        and x.stride(0) % 8 == 0 and x.data_ptr() % 16 == 0
-        and weight.dtype == torch.float32 and weight.dim() == 2 and weight.is_contiguous()
+        x.stride(0) % quantum == 0 and x.data_ptr() % 16 == 0
+        and weight.dtype == torch.float32 and weight.dim() == 2
         and weight.size(0) == x.size(1) and weight.size(1) == 4
         and conv_states.dtype == torch.float32 and conv_states.dim() == 3
-        and conv_states.is_contiguous() and conv_states.size(1) == x.size(1)
-        and conv_states.size(2) == 3
+        and conv_states.size(1) == x.size(1) and 3 <= conv_states.size(2) <= 64
         and part_dim > 0 and part_dim % 64 == 0 and x.size(1) % part_dim == 0
     )
+
+
+def layout_of(x: torch.Tensor, weight: torch.Tensor, conv_states: torch.Tensor) -> KdaConvLayout:
+    """The kda_conv_layout_t describing these tensors."""
+    return make_layout(_DTYPES[x.dtype], conv_states.size(2), conv_states.stride(),
+                       weight.stride())
 
 
 def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None,
@@ -190,20 +240,22 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
                             out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Varlen causal depthwise conv of x (tokens, dim), dim = parts x part_dim.
 
-    Returns (dim // part_dim, tokens, part_dim) bf16; conv_states is updated in
-    place.  `activation` in ("silu", "swish", True) selects SiLU, anything else
-    none.  `null_block_id=None` disables padding detection (the library gets a
-    value no cache index can hold).  `out` may be given to avoid the
-    allocation."""
+    Returns (dim // part_dim, tokens, part_dim) in x's dtype; conv_states is
+    updated in place.  `activation` in ("silu", "swish", True) selects SiLU,
+    anything else none.  `null_block_id=None` disables padding detection (the
+    library gets a value no cache index can hold).  `out` may be given to
+    avoid the allocation."""
     tokens, dim = x.shape
     num_seqs = query_start_loc.numel() - 1
     if out is None:
         out = torch.empty((dim // part_dim, tokens, part_dim), dtype=x.dtype, device=x.device)
     if has_initial_state.dtype != torch.uint8 and has_initial_state.dtype != torch.bool:
         raise TypeError("has_initial_state must be bool or uint8")
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
     act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
-    kda_packed_conv1d(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
-                      cache_indices, has_initial_state, query_start_loc, max(num_seqs, 0), null,
-                      act, out, stream)
+    kda_packed_conv1d_ex(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
+                         cache_indices, has_initial_state, query_start_loc, max(num_seqs, 0),
+                         null, act, out, layout_of(x, weight, conv_states), stream)
     return out

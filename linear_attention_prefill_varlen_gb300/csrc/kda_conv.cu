@@ -1,36 +1,38 @@
 // Packed varlen causal depthwise conv1d (width 4) for GB300 / sm_103a.
 //
 // The operation is the one the vLLM page "vllm.models.kimi_k3.nvidia.ops.kda_conv"
-// describes (module docstring and packed_causal_conv1d_fn): a row-strided bf16
-// x (tokens, dim) is read in place, each channel is convolved causally over its
+// describes (module docstring and packed_causal_conv1d_fn): a row-strided x
+// (tokens, dim) is read in place, each channel is convolved causally over its
 // sequence with 4 FP32 taps (history rows from an FP32 paged conv state), SiLU is
-// optional, and the result is rounded to bf16 (nearest even) into dense
+// optional, and the result is rounded to x's type (nearest even) into dense
 // (tokens, part_dim) planes.  The exact per-element arithmetic is spelled out in
 // include/kda_conv.h.
 //
 // Design (memory-bound stencil, no contraction, so no tensor cores):
-//   * grid = token programs x channel blocks, linearised with the channel block
-//     fastest so that neighbouring CTAs stream neighbouring columns of the same
-//     rows.  A token program p belongs to sequence s with f(s) <= p < f(s+1),
-//     f(s) = floor(qsl[s] / chunk) + s; each sequence owns at least
-//     ceil(len / chunk) programs and the total is at most ceil(tokens/chunk) +
-//     num_seqs (the bound the page's launch uses).  Each warp finds s with a
+//   * The grid is programs x warps-per-program warps, the warp index fastest,
+//     so that neighbouring warps stream neighbouring columns of the same rows.
+//     A program p belongs to sequence s with f(s) <= p < f(s+1),
+//     f(s) = floor(qsl[s] / chunk) + s: each sequence owns at least
+//     ceil(len / chunk) programs and there are ceil(tokens / chunk) + num_seqs
+//     in all (the bound the page's launch uses).  Each warp finds s by a
 //     radix-32 search over query_start_loc (one coalesced 32-candidate probe per
 //     level), so there is no host-side chunk table and the grid depends only on
-//     tokens and num_seqs (graph-safe).
-//   * a thread owns VEC channels (one 16- or 8-byte vector of a row) and walks
-//     the chunk's rows in order: 3 history rows stay in registers as FP32, the
-//     next U rows are loaded one step ahead into a register queue, and every
-//     row is 4 FMAs per channel in a fixed order, the activation, a packed RNE
-//     conversion and one vector store into its plane.
-//   * the first chunk of a sequence reads its conv state and, in the same
-//     thread, writes the updated state (the sequence's last 3 rows, or the
-//     shifted old history for sequences shorter than 3), so there is exactly
-//     one reader and one writer per state line and no ordering between CTAs.
+//     scalar sizes (graph-safe).
+//   * A thread owns VEC channels of its program's rows and walks them in order:
+//     3 history rows stay in registers as FP32, a rolling queue of P raw rows
+//     keeps P loads in flight (a slot is refilled as soon as its row has been
+//     widened), and every row is 4 FMAs per channel in a fixed order, the
+//     activation, a packed round-to-nearest conversion and one vector store.
+//   * The first chunk of a sequence reads its conv state and, in the same
+//     thread, writes the updated state (the last rows of [old state ; the
+//     sequence's rows]), so each state line has exactly one reader and one
+//     writer and no ordering between CTAs is needed.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <type_traits>
@@ -39,7 +41,7 @@
 
 // Launch geometry (compile-time; the defaults are the measured choice on GB300).
 #ifndef KDA_VEC
-#define KDA_VEC 4  // channels per thread: one 8-byte bf16 vector
+#define KDA_VEC 4  // channels per thread
 #endif
 #ifndef KDA_QUEUE
 #define KDA_QUEUE 6  // rows in flight per thread (a multiple of 3 keeps the history in place)
@@ -50,6 +52,9 @@
 #ifndef KDA_MIN_BLOCKS
 #define KDA_MIN_BLOCKS 7  // resident CTAs per SM the register budget is sized for
 #endif
+#ifndef KDA_MIN_BLOCKS_F32
+#define KDA_MIN_BLOCKS_F32 5  // the same for fp32 x (twice the queue registers)
+#endif
 #ifndef KDA_WAVES
 #define KDA_WAVES 1  // waves of resident warps a long prefill is spread over
 #endif
@@ -58,13 +63,6 @@
 #endif
 #ifndef KDA_STORE_CS
 #define KDA_STORE_CS 1  // 1: plane stores use the streaming (evict-first) cache hint
-#endif
-
-#ifndef KDA_LOAD_EVICT_FIRST
-#define KDA_LOAD_EVICT_FIRST 0  // 1: x loads carry an L2 evict-first cache policy
-#endif
-#ifndef KDA_STORE_EVICT_FIRST
-#define KDA_STORE_EVICT_FIRST 0  // 1: plane stores carry an L2 evict-first cache policy
 #endif
 
 #if KDA_LOAD_L2_256
@@ -80,16 +78,24 @@
 
 namespace {
 
+constexpr int kMaxStateWidth = 64;
+
 struct Params {
-    const uint16_t *x;
+    const void *x;
     int64_t x_row_stride;  // elements
     int tokens;
     int dim;
     int part_dim;
     int num_seqs;
     const float *weight;
+    int64_t w_stride_c;  // weight[c][j] at weight[c * w_stride_c + j * w_stride_j]
+    int64_t w_stride_j;
+    bool weight_dense;  // strides (4, 1): one float4 per channel
     const float *bias;
     float *conv_states;
+    int state_width;      // K >= 3; the taps read positions K-3 .. K-1
+    int64_t s_stride[3];  // element strides of conv_states: line, channel, position
+    bool state_dense;     // K == 3 and strides (3 * dim, 3, 1)
     const int32_t *cache_indices;
     const uint8_t *has_initial_state;
     const int32_t *qsl;
@@ -104,52 +110,66 @@ struct Params {
 };
 
 // ---------------------------------------------------------------------------
-// Device helpers
+// Device helpers.  kDtype: KDA_DTYPE_BF16, KDA_DTYPE_F16 or KDA_DTYPE_F32 (the
+// storage of x and out).  A row vector of VEC channels is kept raw, as
+// VEC * bytes / 4 32-bit words.
 // ---------------------------------------------------------------------------
 
-// One row vector of VEC bf16 channels, as VEC/2 32-bit words (channel 2i in the
-// low half of word i).  Streaming load: read once, keep out of L1.
-template <int VEC>
-__device__ __forceinline__ void load_row(const uint16_t *p, uint32_t (&w)[VEC / 2]) {
-    static_assert(VEC == 4 || VEC == 8, "VEC must be 4 or 8");
-#if KDA_LOAD_EVICT_FIRST
-    uint64_t pol;
-    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    if constexpr (VEC == 8) {
-        asm(KDA_LD_X ".L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-            : "l"(p), "l"(pol));
-    } else {
-        asm(KDA_LD_X ".L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
-            : "=r"(w[0]), "=r"(w[1])
-            : "l"(p), "l"(pol));
-    }
-#else
-    if constexpr (VEC == 8) {
-        asm(KDA_LD_X ".v4.u32 {%0, %1, %2, %3}, [%4];"
-            : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-            : "l"(p));
-    } else {
-        asm(KDA_LD_X ".v2.u32 {%0, %1}, [%2];"
-            : "=r"(w[0]), "=r"(w[1])
-            : "l"(p));
-    }
-#endif
+template <int kDtype>
+__host__ __device__ constexpr int elem_bytes() {
+    return kDtype == KDA_DTYPE_F32 ? 4 : 2;
 }
 
-template <int VEC>
-__device__ __forceinline__ void zero_row(uint32_t (&w)[VEC / 2]) {
-#pragma unroll
-    for (int i = 0; i < VEC / 2; ++i) w[i] = 0u;
+template <int VEC, int kDtype>
+__host__ __device__ constexpr int row_words() {
+    return VEC * elem_bytes<kDtype>() / 4;
 }
 
-// bf16 -> fp32 is exact: a bf16 is the upper half of an fp32 bit pattern.
-template <int VEC>
-__device__ __forceinline__ void widen(const uint32_t (&w)[VEC / 2], float (&f)[VEC]) {
+// Streaming load of one raw row vector: read once, kept out of L1.
+template <int W>
+__device__ __forceinline__ void load_row(const void *p, uint32_t (&w)[W]) {
+    static_assert(W == 2 || W % 4 == 0, "row vectors are 8 or 16*n bytes");
+    if constexpr (W == 2) {
+        asm(KDA_LD_X ".v2.u32 {%0, %1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
+    } else {
 #pragma unroll
-    for (int i = 0; i < VEC / 2; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        for (int i = 0; i < W / 4; ++i) {
+            asm(KDA_LD_X ".v4.u32 {%0, %1, %2, %3}, [%4];"
+                : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+                : "l"(static_cast<const char *>(p) + 16 * i));
+        }
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void zero_row(uint32_t (&w)[W]) {
+#pragma unroll
+    for (int i = 0; i < W; ++i) w[i] = 0u;
+}
+
+// Raw row -> FP32, exactly: a bf16 is the upper half of an fp32 bit pattern;
+// every binary16 value is an fp32 value (hardware conversion); fp32 as is.
+template <int VEC, int kDtype>
+__device__ __forceinline__ void widen(const uint32_t (&w)[row_words<VEC, kDtype>()],
+                                      float (&f)[VEC]) {
+    if constexpr (kDtype == KDA_DTYPE_BF16) {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else if constexpr (kDtype == KDA_DTYPE_F16) {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) {
+            __half2 h;
+            memcpy(&h, &w[i], sizeof h);
+            const float2 v = __half22float2(h);
+            f[2 * i] = v.x;
+            f[2 * i + 1] = v.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) f[i] = __uint_as_float(w[i]);
     }
 }
 
@@ -159,6 +179,57 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t u;
     memcpy(&u, &v, sizeof u);
     return u;
+}
+
+// Two fp32 -> one word of two binary16, round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    uint32_t u;
+    memcpy(&u, &v, sizeof u);
+    return u;
+}
+
+template <int W>
+__device__ __forceinline__ void store_words(void *p, const uint32_t (&w)[W]) {
+    if constexpr (W == 2) {
+        asm volatile(KDA_ST_OUT ".v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
+                     : "memory");
+    } else {
+#pragma unroll
+        for (int i = 0; i < W / 4; ++i) {
+            asm volatile(KDA_ST_OUT ".v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(
+                             static_cast<char *>(p) + 16 * i),
+                         "r"(w[4 * i]), "r"(w[4 * i + 1]), "r"(w[4 * i + 2]), "r"(w[4 * i + 3])
+                         : "memory");
+        }
+    }
+}
+
+// FP32 row -> x's type (round to nearest even) -> one vector store.
+template <int VEC, int kDtype>
+__device__ __forceinline__ void store_out_row(void *p, const float (&y)[VEC]) {
+    constexpr int W = row_words<VEC, kDtype>();
+    uint32_t w[W];
+    if constexpr (kDtype == KDA_DTYPE_BF16) {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) w[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
+    } else if constexpr (kDtype == KDA_DTYPE_F16) {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i) w[i] = pack_f16x2(y[2 * i], y[2 * i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) w[i] = __float_as_uint(y[i]);
+    }
+    store_words<W>(p, w);
+}
+
+template <int VEC>
+__device__ __forceinline__ void store_f32_row(float *p, const float (&y)[VEC]) {
+#pragma unroll
+    for (int i = 0; i < VEC / 4; ++i) {
+        reinterpret_cast<float4 *>(p)[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2],
+                                                       y[4 * i + 3]);
+    }
 }
 
 // 2^x and 1/x on the special-function unit (PTX ex2.approx.ftz / rcp.approx.ftz:
@@ -194,46 +265,8 @@ __device__ __forceinline__ void silu_row(float (&y)[VEC]) {
     for (int v = 0; v < VEC; ++v) y[v] = silu_f32(y[v]);
 }
 
-template <int VEC>
-__device__ __forceinline__ void store_bf16_row(uint16_t *p, const float (&y)[VEC]) {
-    uint32_t w[VEC / 2];
-#pragma unroll
-    for (int i = 0; i < VEC / 2; ++i) w[i] = pack_bf16x2(y[2 * i], y[2 * i + 1]);
-#if KDA_STORE_EVICT_FIRST
-    uint64_t pol;
-    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    if constexpr (VEC == 8) {
-        asm volatile(KDA_ST_OUT ".L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
-                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "l"(pol)
-                     : "memory");
-    } else {
-        asm volatile(KDA_ST_OUT ".L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(p), "r"(w[0]),
-                     "r"(w[1]), "l"(pol)
-                     : "memory");
-    }
-#else
-    if constexpr (VEC == 8) {
-        asm volatile(KDA_ST_OUT ".v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-                     "r"(w[2]), "r"(w[3])
-                     : "memory");
-    } else {
-        asm volatile(KDA_ST_OUT ".v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1])
-                     : "memory");
-    }
-#endif
-}
-
-template <int VEC>
-__device__ __forceinline__ void store_f32_row(float *p, const float (&y)[VEC]) {
-#pragma unroll
-    for (int i = 0; i < VEC / 4; ++i) {
-        reinterpret_cast<float4 *>(p)[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2],
-                                                       y[4 * i + 3]);
-    }
-}
-
-// The sequence that owns token program `prog`, or -1 if the program is idle
-// before the first sequence.  Must be called by all 32 lanes of a warp.
+// The sequence that owns program `prog`, or -1 if the program is idle before
+// the first sequence.  Must be called by all 32 lanes of a warp.
 __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane) {
     int base = 0;
     int stride = p.search_top;
@@ -253,9 +286,22 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
 // The conv kernel
 // ---------------------------------------------------------------------------
 
-template <int VEC, int P, bool kPreact, bool kSilu, bool kBias>
-__global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
+// Resident CTAs per SM the register budget is sized for: fp32 rows are twice
+// as wide, so their queue needs more registers.
+template <int kDtype>
+__host__ __device__ constexpr int min_blocks() {
+    return kDtype == KDA_DTYPE_F32 ? KDA_MIN_BLOCKS_F32 : KDA_MIN_BLOCKS;
+}
+
+// kGeneral: the weight and the conv state may have any strides and the state
+// any width K; otherwise both are dense (weight (dim, 4), state (lines, dim, 3)).
+template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
+__global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
     kda_packed_conv1d_kernel(const Params p) {
+    constexpr int W = row_words<VEC, kDtype>();
+    // x and out are addressed in elements of their storage type
+    using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
+    using OT = typename std::conditional<kPreact, float, XT>::type;
     const int lane = threadIdx.x & 31;
     const int64_t gwarp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (gwarp >= p.total_warps) return;  // whole warps only
@@ -282,13 +328,22 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
 
     // Taps and bias of this thread's channels.
     float w[VEC][4];
+    if (!kGeneral || p.weight_dense) {
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-        const float4 q = __ldg(reinterpret_cast<const float4 *>(p.weight) + (c + v));
-        w[v][0] = q.x;
-        w[v][1] = q.y;
-        w[v][2] = q.z;
-        w[v][3] = q.w;
+        for (int v = 0; v < VEC; ++v) {
+            const float4 q = __ldg(reinterpret_cast<const float4 *>(p.weight) + (c + v));
+            w[v][0] = q.x;
+            w[v][1] = q.y;
+            w[v][2] = q.z;
+            w[v][3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                w[v][j] = __ldg(p.weight + (int64_t)(c + v) * p.w_stride_c + j * p.w_stride_j);
+        }
     }
     float bias[VEC];
 #pragma unroll
@@ -301,18 +356,18 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
         bias[4 * i + 3] = q.w;
     }
 
-    const uint16_t *xcol = p.x + c;
+    const XT *xcol = static_cast<const XT *>(p.x) + c;
     const int64_t xs = p.x_row_stride;
 
     // Register queue: slot u holds row t+u; it is refilled with row t+P+u as
     // soon as row t+u has been widened, so P rows are always in flight.
-    uint32_t q[P][VEC / 2];
+    uint32_t q[P][W];
 #pragma unroll
     for (int u = 0; u < P; ++u) {
         if (t0 + u < t1)
-            load_row<VEC>(xcol + (int64_t)(t0 + u) * xs, q[u]);
+            load_row<W>(xcol + (int64_t)(t0 + u) * xs, q[u]);
         else
-            zero_row<VEC>(q[u]);
+            zero_row<W>(q[u]);
     }
 
     // History rows -3, -2, -1 relative to t0 (h0 oldest), in FP32.
@@ -320,69 +375,103 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
     if (k == 0) {
         const int64_t line = __ldg(p.cache_indices + s);
         const bool live = line != p.null_block_id;
-        float st[3 * VEC];
+        const bool read = live && __ldg(p.has_initial_state + s) != 0;
+        const int len = e - a;
+        if (!kGeneral || p.state_dense) {
+            // Width 3, contiguous: a thread's VEC channels are 12*VEC bytes.
+            float st[3 * VEC];
 #pragma unroll
-        for (int i = 0; i < 3 * VEC; ++i) st[i] = 0.0f;
-        float4 *sp = reinterpret_cast<float4 *>(p.conv_states + (line * p.dim + c) * 3);
-        if (live && __ldg(p.has_initial_state + s) != 0) {
+            for (int i = 0; i < 3 * VEC; ++i) st[i] = 0.0f;
+            float4 *sp = reinterpret_cast<float4 *>(p.conv_states + (line * p.dim + c) * 3);
+            if (read) {
 #pragma unroll
-            for (int i = 0; i < 3 * VEC / 4; ++i) {
-                const float4 q = sp[i];
-                st[4 * i] = q.x;
-                st[4 * i + 1] = q.y;
-                st[4 * i + 2] = q.z;
-                st[4 * i + 3] = q.w;
-            }
-        }
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-            h0[v] = st[3 * v];
-            h1[v] = st[3 * v + 1];
-            h2[v] = st[3 * v + 2];
-        }
-        if (live) {
-            // The updated state: the last 3 rows of [history ; rows a .. e-1].
-            const int len = e - a;
-            float ns[3][VEC];
-#pragma unroll
-            for (int r = 0; r < 3; ++r) {
-                const int row = len - 3 + r;
-                if (row >= 0) {
-                    uint32_t raw[VEC / 2];
-                    load_row<VEC>(xcol + (int64_t)(a + row) * xs, raw);
-                    widen<VEC>(raw, ns[r]);
-                } else {
-                    // history index row + 3 = len + r, which is 1 or 2 here
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) ns[r][v] = (len + r == 1) ? h1[v] : h2[v];
+                for (int i = 0; i < 3 * VEC / 4; ++i) {
+                    const float4 v4 = sp[i];
+                    st[4 * i] = v4.x;
+                    st[4 * i + 1] = v4.y;
+                    st[4 * i + 2] = v4.z;
+                    st[4 * i + 3] = v4.w;
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 3 * VEC / 4; ++i) {
-                float o[4];
+            for (int v = 0; v < VEC; ++v) {
+                h0[v] = st[3 * v];
+                h1[v] = st[3 * v + 1];
+                h2[v] = st[3 * v + 2];
+            }
+            if (live) {
+                // The updated state: the last 3 rows of [history ; rows a .. e-1].
+                float ns[3][VEC];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int flat = 4 * i + j;  // = 3 * channel + state index
-                    o[j] = ns[flat % 3][flat / 3];
+                for (int r = 0; r < 3; ++r) {
+                    const int row = len - 3 + r;
+                    if (row >= 0) {
+                        uint32_t raw[W];
+                        load_row<W>(xcol + (int64_t)(a + row) * xs, raw);
+                        widen<VEC, kDtype>(raw, ns[r]);
+                    } else {
+                        // history index row + 3 = len + r, which is 1 or 2 here
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v) ns[r][v] = (len + r == 1) ? h1[v] : h2[v];
+                    }
                 }
-                sp[i] = make_float4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+                for (int i = 0; i < 3 * VEC / 4; ++i) {
+                    float o4[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int flat = 4 * i + j;  // = 3 * channel + state index
+                        o4[j] = ns[flat % 3][flat / 3];
+                    }
+                    sp[i] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+        } else {
+            // Any width K and strides: positions K-3 .. K-1 feed the taps; the
+            // update keeps the last K rows of [old line ; the sequence's rows].
+            // Ascending positions read position kk + len before it is written.
+            const int K = p.state_width;
+            const int64_t s0 = p.s_stride[0], s1 = p.s_stride[1], s2 = p.s_stride[2];
+            float *base = p.conv_states + line * s0 + (int64_t)c * s1;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                h0[v] = read ? base[v * s1 + (K - 3) * s2] : 0.0f;
+                h1[v] = read ? base[v * s1 + (K - 2) * s2] : 0.0f;
+                h2[v] = read ? base[v * s1 + (K - 1) * s2] : 0.0f;
+            }
+            if (live) {
+                for (int kk = 0; kk < K; ++kk) {
+                    const int row = len - K + kk;
+                    float vals[VEC];
+                    if (row >= 0) {
+                        uint32_t raw[W];
+                        load_row<W>(xcol + (int64_t)(a + row) * xs, raw);
+                        widen<VEC, kDtype>(raw, vals);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < VEC; ++v)
+                            vals[v] = read ? base[v * s1 + (int64_t)(kk + len) * s2] : 0.0f;
+                    }
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) base[v * s1 + (int64_t)kk * s2] = vals[v];
+                }
             }
         }
     } else {
-        uint32_t raw[VEC / 2];
-        load_row<VEC>(xcol + (int64_t)(t0 - 3) * xs, raw);
-        widen<VEC>(raw, h0);
-        load_row<VEC>(xcol + (int64_t)(t0 - 2) * xs, raw);
-        widen<VEC>(raw, h1);
-        load_row<VEC>(xcol + (int64_t)(t0 - 1) * xs, raw);
-        widen<VEC>(raw, h2);
+        uint32_t raw[W];
+        load_row<W>(xcol + (int64_t)(t0 - 3) * xs, raw);
+        widen<VEC, kDtype>(raw, h0);
+        load_row<W>(xcol + (int64_t)(t0 - 2) * xs, raw);
+        widen<VEC, kDtype>(raw, h1);
+        load_row<W>(xcol + (int64_t)(t0 - 1) * xs, raw);
+        widen<VEC, kDtype>(raw, h2);
     }
 
     const int plane = c / p.part_dim;
     const int col = c - plane * p.part_dim;
-    const int64_t out_row = p.part_dim;
+    const int64_t out_row = p.part_dim;  // elements between output rows
     int64_t o = (int64_t)plane * p.plane_stride + col + (int64_t)t0 * out_row;
-    const uint16_t *xnext = xcol + (int64_t)(t0 + P) * xs;
+    const XT *xnext = xcol + (int64_t)(t0 + P) * xs;
 
     // P rows per step.  Steps whose rows and refills all lie inside the chunk
     // run without per-row bounds checks; the last one or two steps check.
@@ -392,8 +481,8 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
 #pragma unroll
         for (int u = 0; u < P; ++u) {
             float xv[VEC];
-            widen<VEC>(q[u], xv);
-            if (!kChecked || t + P + u < t1) load_row<VEC>(xnext + (int64_t)u * xs, q[u]);
+            widen<VEC, kDtype>(q[u], xv);
+            if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
             float y[VEC];
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
@@ -409,10 +498,11 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
             }
             if constexpr (kSilu) silu_row<VEC>(y);
             if (!kChecked || t + u < t1) {
+                OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
                 if constexpr (kPreact)
-                    store_f32_row<VEC>(static_cast<float *>(p.out) + o + u * out_row, y);
+                    store_f32_row<VEC>(dst, y);
                 else
-                    store_bf16_row<VEC>(static_cast<uint16_t *>(p.out) + o + u * out_row, y);
+                    store_out_row<VEC, kDtype>(dst, y);
             }
         }
         xnext += P * xs;
@@ -423,8 +513,8 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, KDA_MIN_BLOCKS)
 }
 
 // The epilogue alone, over consecutive fp32 bit patterns, VEC at a time
-// through the same row functions as the conv kernel.  mode 0: rounding only;
-// 1: SiLU, then rounding.
+// through the same row functions as the conv kernel (bf16 output).
+// kMode 0: rounding only; 1: SiLU, then rounding.
 template <int VEC, int kMode>
 __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first, uint64_t count,
                                                                  uint16_t *out) {
@@ -436,7 +526,7 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
         for (int v = 0; v < VEC; ++v) y[v] = __uint_as_float(first + (uint32_t)(i + v));
         if constexpr (kMode == 1) silu_row<VEC>(y);
         if (i + VEC <= count) {
-            store_bf16_row<VEC>(out + i, y);
+            store_out_row<VEC, KDA_DTYPE_BF16>(out + i, y);
         } else {
             for (int v = 0; v < VEC && i + v < count; v += 2) {
                 const uint32_t wd = pack_bf16x2(y[v], y[v + 1]);
@@ -456,12 +546,26 @@ thread_local char g_last_error[256] = "";
 constexpr int kVec = KDA_VEC;                 // channels per thread
 constexpr int kQueue = KDA_QUEUE;             // rows in flight per thread
 constexpr int kThreads = KDA_CTA_THREADS;
-constexpr int kWarpsPerSm = KDA_CTA_THREADS / 32 * KDA_MIN_BLOCKS;
 constexpr int kDefaultSms = 152;              // GB300, for shape queries without a device
 constexpr int kMinChunk = 2 * KDA_QUEUE;
 constexpr int kMaxChunk = 2048;
 
-bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool aligned(const void *ptr, uintptr_t bytes) {
+    return (reinterpret_cast<uintptr_t>(ptr) & (bytes - 1)) == 0;
+}
+
+// The layout a NULL layout pointer stands for: bf16, width 3, contiguous.
+kda_conv_layout_t default_layout(int64_t dim) {
+    kda_conv_layout_t l;
+    l.x_dtype = KDA_DTYPE_BF16;
+    l.state_width = 3;
+    l.state_stride[0] = 3 * dim;
+    l.state_stride[1] = 3;
+    l.state_stride[2] = 1;
+    l.weight_stride[0] = 4;
+    l.weight_stride[1] = 1;
+    return l;
+}
 
 kda_status_t check_sizes(int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
                          int64_t num_seqs) {
@@ -473,20 +577,39 @@ kda_status_t check_sizes(int64_t x_row_stride, int64_t tokens, int64_t dim, int6
     return KDA_OK;
 }
 
+bool state_is_dense(const kda_conv_layout_t &l, int64_t dim) {
+    return l.state_width == 3 && l.state_stride[0] == 3 * dim && l.state_stride[1] == 3 &&
+           l.state_stride[2] == 1;
+}
+
+bool weight_is_dense(const kda_conv_layout_t &l) {
+    return l.weight_stride[0] == 4 && l.weight_stride[1] == 1;
+}
+
 kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
                         int64_t part_dim, const float *weight, const float *bias,
                         const float *conv_states, const int32_t *cache_indices,
                         const uint8_t *has_initial_state, const int32_t *query_start_loc,
-                        int64_t num_seqs, int activation, const void *out) {
+                        int64_t num_seqs, int activation, const void *out,
+                        const kda_conv_layout_t &l) {
     kda_status_t st = check_sizes(x_row_stride, tokens, dim, part_dim, num_seqs);
     if (st != KDA_OK) return st;
     if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
+    if (l.x_dtype != KDA_DTYPE_BF16 && l.x_dtype != KDA_DTYPE_F16 && l.x_dtype != KDA_DTYPE_F32)
+        return KDA_ERR_INVALID_ARG;
+    if (l.state_width < 3) return KDA_ERR_INVALID_ARG;
+    if (l.state_width > kMaxStateWidth) return KDA_ERR_UNSUPPORTED;
     if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;  // nothing is touched
     if (!x || !weight || !conv_states || !cache_indices || !has_initial_state ||
         !query_start_loc || !out)
         return KDA_ERR_INVALID_ARG;
-    if (!aligned16(x) || x_row_stride % 8 != 0 || !aligned16(weight) ||
-        (bias && !aligned16(bias)) || !aligned16(conv_states) || !aligned16(out))
+    // rows of x must start on 16-byte boundaries: 8 elements of 2 bytes, 4 of 4
+    const int64_t row_quantum = l.x_dtype == KDA_DTYPE_F32 ? 4 : 8;
+    if (!aligned(x, 16) || x_row_stride % row_quantum != 0 || !aligned(out, 16) ||
+        (bias && !aligned(bias, 16)))
+        return KDA_ERR_MISALIGNED;
+    if (weight_is_dense(l) ? !aligned(weight, 16) : !aligned(weight, 4)) return KDA_ERR_MISALIGNED;
+    if (state_is_dense(l, dim) ? !aligned(conv_states, 16) : !aligned(conv_states, 4))
         return KDA_ERR_MISALIGNED;
     return KDA_OK;
 }
@@ -507,12 +630,13 @@ struct Shape {
 // exceeds the budget, the chunk that spreads the tokens over the budget.
 // Clamped to [kMinChunk, kMaxChunk].  It depends only on the scalar sizes and
 // the SM count, so a captured launch stays valid for new metadata.
-Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms) {
+Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
+                   int blocks_per_sm = KDA_MIN_BLOCKS) {
     Shape sh{};
     sh.threads = kThreads;
     const int64_t nvec = dim / kVec;
     sh.warps_per_prog = (int)((nvec + 31) / 32);
-    const int64_t slots = (int64_t)KDA_WAVES * sms * kWarpsPerSm;
+    const int64_t slots = (int64_t)KDA_WAVES * sms * (kThreads / 32) * blocks_per_sm;
     const int64_t max_programs = slots / sh.warps_per_prog;
     int64_t chunk;
     if (max_programs > num_seqs) {
@@ -545,35 +669,78 @@ int current_sms() {
     return cache[dev];
 }
 
-template <bool kPreact, bool kSilu, bool kBias>
+template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
 void launch(const Params &p, const Shape &sh, cudaStream_t stream) {
-    kda_packed_conv1d_kernel<kVec, kQueue, kPreact, kSilu, kBias>
+    kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias>
         <<<(unsigned)sh.ctas, sh.threads, 0, stream>>>(p);
+}
+
+template <int kDtype, bool kGeneral>
+void dispatch_act(const Params &p, const Shape &sh, bool silu, cudaStream_t s) {
+    if (silu) {
+        if (p.bias)
+            launch<kDtype, kGeneral, false, true, true>(p, sh, s);
+        else
+            launch<kDtype, kGeneral, false, true, false>(p, sh, s);
+    } else {
+        if (p.bias)
+            launch<kDtype, kGeneral, false, false, true>(p, sh, s);
+        else
+            launch<kDtype, kGeneral, false, false, false>(p, sh, s);
+    }
+}
+
+template <int kDtype>
+void dispatch(const Params &p, const Shape &sh, bool silu, cudaStream_t s) {
+    if (p.weight_dense && p.state_dense)
+        dispatch_act<kDtype, false>(p, sh, silu, s);
+    else
+        dispatch_act<kDtype, true>(p, sh, silu, s);
+}
+
+kda_status_t record_cuda_error() {
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) {
+        snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
+                 cudaGetErrorString(err));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
 }
 
 kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
                  int64_t part_dim, const float *weight, const float *bias, float *conv_states,
                  const int32_t *cache_indices, const uint8_t *has_initial_state,
                  const int32_t *query_start_loc, int64_t num_seqs, int64_t null_block_id,
-                 int activation, void *out, bool preact, kda_stream_t stream) {
+                 int activation, void *out, bool preact, const kda_conv_layout_t *layout,
+                 kda_stream_t stream) {
+    const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
     kda_status_t st = check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
                                  cache_indices, has_initial_state, query_start_loc, num_seqs,
-                                 activation, out);
+                                 activation, out, l);
     if (st != KDA_OK) return st;
     if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;
 
-    const Shape sh = launch_shape(tokens, dim, num_seqs, current_sms());
+    const int blocks_per_sm =
+        l.x_dtype == KDA_DTYPE_F32 ? min_blocks<KDA_DTYPE_F32>() : min_blocks<KDA_DTYPE_BF16>();
+    const Shape sh = launch_shape(tokens, dim, num_seqs, current_sms(), blocks_per_sm);
     if (sh.ctas > INT32_MAX) return KDA_ERR_INVALID_ARG;
     Params p;
-    p.x = static_cast<const uint16_t *>(x);
+    p.x = x;
     p.x_row_stride = x_row_stride;
     p.tokens = (int)tokens;
     p.dim = (int)dim;
     p.part_dim = (int)part_dim;
     p.num_seqs = (int)num_seqs;
     p.weight = weight;
+    p.w_stride_c = l.weight_stride[0];
+    p.w_stride_j = l.weight_stride[1];
+    p.weight_dense = weight_is_dense(l);
     p.bias = bias;
     p.conv_states = conv_states;
+    p.state_width = l.state_width;
+    for (int i = 0; i < 3; ++i) p.s_stride[i] = l.state_stride[i];
+    p.state_dense = state_is_dense(l, dim);
     p.cache_indices = cache_indices;
     p.has_initial_state = has_initial_state;
     p.qsl = query_start_loc;
@@ -593,30 +760,19 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.search_top = steps > 0 ? (int)(reach / 32) : 1;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool silu = activation == KDA_ACT_SILU;
-    if (preact) {
+    if (preact) {  // bf16 x and the default layout only
         if (bias)
-            launch<true, false, true>(p, sh, s);
+            launch<KDA_DTYPE_BF16, false, true, false, true>(p, sh, s);
         else
-            launch<true, false, false>(p, sh, s);
-    } else if (silu) {
-        if (bias)
-            launch<false, true, true>(p, sh, s);
-        else
-            launch<false, true, false>(p, sh, s);
+            launch<KDA_DTYPE_BF16, false, true, false, false>(p, sh, s);
+    } else if (l.x_dtype == KDA_DTYPE_F16) {
+        dispatch<KDA_DTYPE_F16>(p, sh, activation == KDA_ACT_SILU, s);
+    } else if (l.x_dtype == KDA_DTYPE_F32) {
+        dispatch<KDA_DTYPE_F32>(p, sh, activation == KDA_ACT_SILU, s);
     } else {
-        if (bias)
-            launch<false, false, true>(p, sh, s);
-        else
-            launch<false, false, false>(p, sh, s);
+        dispatch<KDA_DTYPE_BF16>(p, sh, activation == KDA_ACT_SILU, s);
     }
-    const cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) {
-        snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
-                 cudaGetErrorString(err));
-        return KDA_ERR_CUDA;
-    }
-    return KDA_OK;
+    return record_cuda_error();
 }
 
 }  // namespace
@@ -631,7 +787,19 @@ kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t toke
                                kda_stream_t stream) {
     return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
                has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
-               false, stream);
+               false, nullptr, stream);
+}
+
+kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t tokens,
+                                  int64_t dim, int64_t part_dim, const float *weight,
+                                  const float *bias, float *conv_states,
+                                  const int32_t *cache_indices, const uint8_t *has_initial_state,
+                                  const int32_t *query_start_loc, int64_t num_seqs,
+                                  int64_t null_block_id, int activation, void *out,
+                                  const kda_conv_layout_t *layout, kda_stream_t stream) {
+    return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
+               has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
+               false, layout, stream);
 }
 
 kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, int64_t tokens,
@@ -643,7 +811,7 @@ kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, i
                                           int64_t null_block_id, float *out, kda_stream_t stream) {
     return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
                has_initial_state, query_start_loc, num_seqs, null_block_id, KDA_ACT_NONE, out,
-               true, stream);
+               true, nullptr, stream);
 }
 
 kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, int64_t tokens,
@@ -655,7 +823,18 @@ kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, i
                                           int activation, const void *out) {
     return check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
                       cache_indices, has_initial_state, query_start_loc, num_seqs, activation,
-                      out);
+                      out, default_layout(dim));
+}
+
+kda_status_t kda_packed_conv1d_ex_check_args(
+    const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
+    const float *weight, const float *bias, const float *conv_states,
+    const int32_t *cache_indices, const uint8_t *has_initial_state,
+    const int32_t *query_start_loc, int64_t num_seqs, int activation, const void *out,
+    const kda_conv_layout_t *layout) {
+    return check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
+                      cache_indices, has_initial_state, query_start_loc, num_seqs, activation,
+                      out, layout ? *layout : default_layout(dim));
 }
 
 kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t part_dim,
@@ -664,8 +843,8 @@ kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t
                                             int64_t *programs) {
     kda_status_t st = check_sizes(dim, tokens, dim, part_dim, num_seqs);
     if (st != KDA_OK) return st;
-    Shape sh{};
     if (sm_count < 0) return KDA_ERR_INVALID_ARG;
+    Shape sh{};
     if (tokens > 0 && num_seqs > 0 && dim > 0)
         sh = launch_shape(tokens, dim, num_seqs, sm_count > 0 ? sm_count : current_sms());
     if (ctas) *ctas = sh.ctas;
@@ -724,7 +903,7 @@ kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, 
     if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
     if (count == 0) return KDA_OK;
     if (!out) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(out)) return KDA_ERR_MISALIGNED;
+    if (!aligned(out, 16)) return KDA_ERR_MISALIGNED;
     const uint64_t groups = (count + kVec - 1) / kVec;
     const unsigned threads = 256;
     const uint64_t want = (groups + threads - 1) / threads;
@@ -734,21 +913,15 @@ kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, 
         kda_epilogue_range_kernel<kVec, 1><<<blocks, threads, 0, s>>>(first, count, out);
     else
         kda_epilogue_range_kernel<kVec, 0><<<blocks, threads, 0, s>>>(first, count, out);
-    const cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) {
-        snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
-                 cudaGetErrorString(err));
-        return KDA_ERR_CUDA;
-    }
-    return KDA_OK;
+    return record_cuda_error();
 }
 
 const char *kda_status_string(kda_status_t status) {
     switch (status) {
         case KDA_OK: return "ok";
         case KDA_ERR_INVALID_ARG: return "invalid argument";
-        case KDA_ERR_UNSUPPORTED: return "unsupported shape (part_dim % 64 or dim % part_dim)";
-        case KDA_ERR_MISALIGNED: return "misaligned pointer or row stride (16-byte rule)";
+        case KDA_ERR_UNSUPPORTED: return "unsupported shape or layout";
+        case KDA_ERR_MISALIGNED: return "misaligned pointer or row stride";
         case KDA_ERR_CUDA: return "CUDA launch error";
         case KDA_ERR_METADATA: return "malformed metadata";
     }

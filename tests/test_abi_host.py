@@ -161,3 +161,40 @@ def test_validate_metadata(kda):
         st, where = kda.validate_metadata(torch.tensor(qsl), torch.tensor(ci), 8, 4, -1)
         assert st == kda.KDA_ERR_METADATA and where == bad, (qsl, ci, st, where)
     assert kda.validate_metadata(torch.tensor([0, 2, 5]), torch.tensor([-1, -1]), 8, 4, -1)[0] == 0
+
+
+def _layout(kda, dtype=0, width=3, sstride=(3 * 4608, 3, 1), wstride=(4, 1)):
+    return kda.make_layout(dtype, width, sstride, wstride)
+
+
+@pytest.mark.parametrize("lay,over,status", [
+    ({}, {}, 0),
+    ({"dtype": 1}, {}, 0),
+    ({"dtype": 2}, {}, 0),
+    ({"dtype": 3}, {}, 1),
+    ({"width": 2}, {}, 1),
+    ({"width": 65}, {}, 2),
+    ({"width": 8, "sstride": (8, 8 * 100000, 1)}, {}, 0),
+    ({"dtype": 2}, {"x_row_stride": 6404}, 0),  # fp32 rows: 16 bytes = 4 elements
+    ({"dtype": 1}, {"x_row_stride": 6404}, 3),  # fp16 rows: 8 elements
+    ({"wstride": (1, 4608)}, {"weight": A16 + 4}, 0),  # strided weight: 4-byte alignment
+    ({}, {"weight": A16 + 4}, 3),  # dense weight: 16-byte alignment
+    ({"sstride": (3 * 4608, 1, 4608)}, {"conv_states": A16 + 4}, 0),
+    ({}, {"conv_states": A16 + 4}, 3),
+    ({"sstride": (3 * 4608, 1, 4608)}, {"conv_states": A16 + 2}, 3),
+])
+def test_layout_checks(kda, lay, over, status):
+    a = good_args(**over)
+    st = kda.check_args_ex(a["x"], a["x_row_stride"], a["tokens"], a["dim"], a["part_dim"],
+                           a["weight"], a["bias"], a["conv_states"], a["cache_indices"],
+                           a["has_initial_state"], a["query_start_loc"], a["num_seqs"],
+                           a["activation"], a["out"], _layout(kda, **lay))
+    assert st == status
+
+
+def test_null_layout_is_the_default(kda):
+    a = good_args(weight=A16 + 4)
+    args = (a["x"], a["x_row_stride"], a["tokens"], a["dim"], a["part_dim"], a["weight"],
+            a["bias"], a["conv_states"], a["cache_indices"], a["has_initial_state"],
+            a["query_start_loc"], a["num_seqs"], a["activation"], a["out"])
+    assert kda.check_args_ex(*args, None) == kda.check_args(*args) == 3
