@@ -144,6 +144,26 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
                                   const kda_conv_layout_t *layout, kda_stream_t stream);
 
 /*
+ * kda_conv1d_update -- the decode-shaped case: token i (row i of x, i < batch) is
+ * the next row of the sequence whose conv state is line cache_indices[i]. It is
+ * kda_packed_conv1d with query_start_loc = 0, 1, ..., batch and every
+ * has_initial_state set, computed without the program search: one thread per
+ * (token, channel vector) reads the line's 3 newest rows, writes one output row
+ * out[c / part_dim][i][c % part_dim] and the line shifted by one row (the oldest
+ * dropped, x appended). A token whose cache index is null_block_id is computed
+ * with a zero history and its line is not touched. The decode-step counterpart of
+ * the conv update the kda_decode page's fused decode kernel performs. Layout as
+ * for kda_packed_conv1d_ex (NULL: bf16, width 3, contiguous). Cache indices must
+ * be distinct (or null); out must not overlap x or conv_states. Asynchronous on
+ * `stream`; allocates nothing.
+ */
+kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
+                              int64_t part_dim, const float *weight, const float *bias,
+                              float *conv_states, const int32_t *cache_indices,
+                              int64_t null_block_id, int activation, void *out,
+                              const kda_conv_layout_t *layout, kda_stream_t stream);
+
+/*
  * kda_packed_conv1d_preact_f32 -- the same conv without activation or rounding:
  * `out` receives the FP32 accumulator (dim/part_dim, tokens, part_dim) and the conv
  * state is updated exactly as by kda_packed_conv1d. Same arguments and rules as

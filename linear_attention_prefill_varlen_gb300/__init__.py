@@ -22,7 +22,9 @@ from ._binding import (  # noqa: F401
     KDA_OK,
     KdaConvLayout,
     KdaError,
+    causal_conv1d_update,
     epilogue_range,
+    kda_conv1d_update,
     kda_packed_conv1d,
     kda_packed_conv1d_ex,
     kda_packed_conv1d_preact_f32,

@@ -56,6 +56,8 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     handle.kda_packed_conv1d.argtypes = conv + [C, P, P]
     handle.kda_packed_conv1d_preact_f32.argtypes = conv + [P, P]
     handle.kda_packed_conv1d_ex.argtypes = conv + [C, P, ctypes.POINTER(KdaConvLayout), P]
+    handle.kda_conv1d_update.argtypes = [P, I64, I64, I64, I64, P, P, P, P, I64, C, P,
+                                         ctypes.POINTER(KdaConvLayout), P]
     handle.kda_packed_conv1d_ex_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P,
                                                        I64, C, P, ctypes.POINTER(KdaConvLayout)]
     handle.kda_packed_conv1d_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64,
@@ -66,6 +68,7 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     handle.kda_validate_metadata.argtypes = [P, P, I64, I64, I64, I64, ctypes.POINTER(I64)]
     handle.kda_epilogue_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, C, P, P]
     for name in ("kda_packed_conv1d", "kda_packed_conv1d_preact_f32", "kda_packed_conv1d_ex",
+                 "kda_conv1d_update",
                  "kda_packed_conv1d_ex_check_args",
                  "kda_packed_conv1d_check_args", "kda_packed_conv1d_launch_shape",
                  "kda_validate_metadata", "kda_epilogue_range"):
@@ -140,6 +143,35 @@ def kda_packed_conv1d_ex(x, x_row_stride: int, tokens: int, dim: int, part_dim: 
         _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
         num_seqs, null_block_id, activation, _ptr(out),
         None if layout is None else ctypes.byref(layout), _stream(stream)))
+
+
+def kda_conv1d_update(x, x_row_stride: int, batch: int, dim: int, part_dim: int, weight, bias,
+                      conv_states, cache_indices, null_block_id: int, activation: int, out,
+                      layout: KdaConvLayout | None = None, stream=None) -> None:
+    """C-ABI kda_conv1d_update: one new token per sequence (decode)."""
+    _check(lib().kda_conv1d_update(
+        _ptr(x), x_row_stride, batch, dim, part_dim, _ptr(weight), _ptr(bias), _ptr(conv_states),
+        _ptr(cache_indices), null_block_id, activation, _ptr(out),
+        None if layout is None else ctypes.byref(layout), _stream(stream)))
+
+
+def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: torch.Tensor,
+                         bias: torch.Tensor | None, cache_indices: torch.Tensor, part_dim: int,
+                         activation="silu", null_block_id: int | None = None,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode step: x (batch, dim), row i the next token of the sequence at
+    conv-state line cache_indices[i].  Returns (dim // part_dim, batch, part_dim)
+    in x's dtype and shifts each touched line by one row, in place."""
+    batch, dim = x.shape
+    if out is None:
+        out = torch.empty((dim // part_dim, batch, part_dim), dtype=x.dtype, device=x.device)
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
+    act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
+    null = -(2 ** 62) if null_block_id is None else int(null_block_id)
+    kda_conv1d_update(x, x.stride(0), batch, dim, part_dim, weight, bias, conv_states,
+                      cache_indices, null, act, out, layout_of(x, weight, conv_states), stream)
+    return out
 
 
 def check_args_ex(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,

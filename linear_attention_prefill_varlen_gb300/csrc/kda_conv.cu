@@ -538,6 +538,134 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 }
 
 // ---------------------------------------------------------------------------
+// The decode-shaped update: token i is the next row of the sequence whose conv
+// state is line cache_indices[i].  One thread per (token, channel vector): read
+// the line's 3 newest rows, one row of x, write one output row and the line
+// shifted by one row.  No program search: the grid is tokens x vectors.
+// ---------------------------------------------------------------------------
+
+template <int VEC, int kDtype, bool kGeneral, bool kSilu, bool kBias>
+__global__ void __launch_bounds__(256, 4) kda_conv1d_update_kernel(const Params p) {
+    constexpr int W = row_words<VEC, kDtype>();
+    using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
+    const int64_t nvec = p.dim / VEC;
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t token = gid / nvec;
+    if (token >= p.tokens) return;
+    const int c = (int)(gid - token * nvec) * VEC;
+
+    float w[VEC][4];
+    if (!kGeneral || p.weight_dense) {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            const float4 q = __ldg(reinterpret_cast<const float4 *>(p.weight) + (c + v));
+            w[v][0] = q.x;
+            w[v][1] = q.y;
+            w[v][2] = q.z;
+            w[v][3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                w[v][j] = __ldg(p.weight + (int64_t)(c + v) * p.w_stride_c + j * p.w_stride_j);
+        }
+    }
+    float bias[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC / 4; ++i) {
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (kBias) q = __ldg(reinterpret_cast<const float4 *>(p.bias + c) + i);
+        bias[4 * i] = q.x;
+        bias[4 * i + 1] = q.y;
+        bias[4 * i + 2] = q.z;
+        bias[4 * i + 3] = q.w;
+    }
+
+    uint32_t raw[W];
+    load_row<W>(static_cast<const XT *>(p.x) + token * p.x_row_stride + c, raw);
+    float xv[VEC];
+    widen<VEC, kDtype>(raw, xv);
+
+    const int64_t line = __ldg(p.cache_indices + token);
+    const bool live = line != p.null_block_id;
+    float h0[VEC], h1[VEC], h2[VEC];
+    if (!kGeneral || p.state_dense) {
+        float4 *sp = reinterpret_cast<float4 *>(p.conv_states + (line * p.dim + c) * 3);
+        float st[3 * VEC];
+#pragma unroll
+        for (int i = 0; i < 3 * VEC; ++i) st[i] = 0.0f;
+        if (live) {
+#pragma unroll
+            for (int i = 0; i < 3 * VEC / 4; ++i) {
+                const float4 v4 = sp[i];
+                st[4 * i] = v4.x;
+                st[4 * i + 1] = v4.y;
+                st[4 * i + 2] = v4.z;
+                st[4 * i + 3] = v4.w;
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            h0[v] = st[3 * v];
+            h1[v] = st[3 * v + 1];
+            h2[v] = st[3 * v + 2];
+        }
+        if (live) {
+            // new line: (h1, h2, x) per channel
+#pragma unroll
+            for (int i = 0; i < 3 * VEC / 4; ++i) {
+                float o4[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int flat = 4 * i + j;
+                    const int v = flat / 3, r = flat % 3;
+                    o4[j] = r == 0 ? h1[v] : (r == 1 ? h2[v] : xv[v]);
+                }
+                sp[i] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            }
+        }
+    } else {
+        const int K = p.state_width;
+        const int64_t s1 = p.s_stride[1], s2 = p.s_stride[2];
+        float *base = p.conv_states + line * p.s_stride[0] + (int64_t)c * s1;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) {
+            h0[v] = live ? base[v * s1 + (K - 3) * s2] : 0.0f;
+            h1[v] = live ? base[v * s1 + (K - 2) * s2] : 0.0f;
+            h2[v] = live ? base[v * s1 + (K - 1) * s2] : 0.0f;
+        }
+        if (live) {
+            // shift by one row (ascending: position kk + 1 is read before it is
+            // overwritten), then the new row at position K-1
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+                for (int kk = 0; kk + 1 < K; ++kk)
+                    base[v * s1 + (int64_t)kk * s2] = base[v * s1 + (int64_t)(kk + 1) * s2];
+                base[v * s1 + (int64_t)(K - 1) * s2] = xv[v];
+            }
+        }
+    }
+
+    float y[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        float acc = kBias ? bias[v] : 0.0f;
+        acc = __fmaf_rn(h0[v], w[v][0], acc);
+        acc = __fmaf_rn(h1[v], w[v][1], acc);
+        acc = __fmaf_rn(h2[v], w[v][2], acc);
+        acc = __fmaf_rn(xv[v], w[v][3], acc);
+        y[v] = acc;
+    }
+    if constexpr (kSilu) silu_row<VEC>(y);
+    const int plane = c / p.part_dim;
+    const int col = c - plane * p.part_dim;
+    store_out_row<VEC, kDtype>(
+        static_cast<XT *>(p.out) + (int64_t)plane * p.plane_stride + token * p.part_dim + col, y);
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -591,7 +719,7 @@ kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int
                         const float *conv_states, const int32_t *cache_indices,
                         const uint8_t *has_initial_state, const int32_t *query_start_loc,
                         int64_t num_seqs, int activation, const void *out,
-                        const kda_conv_layout_t &l) {
+                        const kda_conv_layout_t &l, bool need_ranges = true) {
     kda_status_t st = check_sizes(x_row_stride, tokens, dim, part_dim, num_seqs);
     if (st != KDA_OK) return st;
     if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
@@ -600,9 +728,8 @@ kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int
     if (l.state_width < 3) return KDA_ERR_INVALID_ARG;
     if (l.state_width > kMaxStateWidth) return KDA_ERR_UNSUPPORTED;
     if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;  // nothing is touched
-    if (!x || !weight || !conv_states || !cache_indices || !has_initial_state ||
-        !query_start_loc || !out)
-        return KDA_ERR_INVALID_ARG;
+    if (!x || !weight || !conv_states || !cache_indices || !out) return KDA_ERR_INVALID_ARG;
+    if (need_ranges && (!has_initial_state || !query_start_loc)) return KDA_ERR_INVALID_ARG;
     // rows of x must start on 16-byte boundaries: 8 elements of 2 bytes, 4 of 4
     const int64_t row_quantum = l.x_dtype == KDA_DTYPE_F32 ? 4 : 8;
     if (!aligned(x, 16) || x_row_stride % row_quantum != 0 || !aligned(out, 16) ||
@@ -775,6 +902,80 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     return record_cuda_error();
 }
 
+template <int kDtype, bool kGeneral, bool kSilu, bool kBias>
+void launch_update(const Params &p, int64_t blocks, cudaStream_t stream) {
+    kda_conv1d_update_kernel<kVec, kDtype, kGeneral, kSilu, kBias>
+        <<<(unsigned)blocks, 256, 0, stream>>>(p);
+}
+
+template <int kDtype, bool kGeneral>
+void dispatch_update_act(const Params &p, int64_t blocks, bool silu, cudaStream_t s) {
+    if (silu) {
+        if (p.bias)
+            launch_update<kDtype, kGeneral, true, true>(p, blocks, s);
+        else
+            launch_update<kDtype, kGeneral, true, false>(p, blocks, s);
+    } else {
+        if (p.bias)
+            launch_update<kDtype, kGeneral, false, true>(p, blocks, s);
+        else
+            launch_update<kDtype, kGeneral, false, false>(p, blocks, s);
+    }
+}
+
+template <int kDtype>
+void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s) {
+    if (p.weight_dense && p.state_dense)
+        dispatch_update_act<kDtype, false>(p, blocks, silu, s);
+    else
+        dispatch_update_act<kDtype, true>(p, blocks, silu, s);
+}
+
+kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
+                        int64_t part_dim, const float *weight, const float *bias,
+                        float *conv_states, const int32_t *cache_indices, int64_t null_block_id,
+                        int activation, void *out, const kda_conv_layout_t *layout,
+                        kda_stream_t stream) {
+    const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
+    kda_status_t st = check_args(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
+                                 cache_indices, nullptr, nullptr, batch, activation, out, l,
+                                 false);
+    if (st != KDA_OK) return st;
+    if (batch == 0 || dim == 0) return KDA_OK;
+    const int64_t threads_total = batch * (dim / kVec);
+    const int64_t blocks = (threads_total + 255) / 256;
+    if (blocks > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    Params p{};
+    p.x = x;
+    p.x_row_stride = x_row_stride;
+    p.tokens = (int)batch;
+    p.dim = (int)dim;
+    p.part_dim = (int)part_dim;
+    p.num_seqs = (int)batch;
+    p.weight = weight;
+    p.w_stride_c = l.weight_stride[0];
+    p.w_stride_j = l.weight_stride[1];
+    p.weight_dense = weight_is_dense(l);
+    p.bias = bias;
+    p.conv_states = conv_states;
+    p.state_width = l.state_width;
+    for (int i = 0; i < 3; ++i) p.s_stride[i] = l.state_stride[i];
+    p.state_dense = state_is_dense(l, dim);
+    p.cache_indices = cache_indices;
+    p.null_block_id = null_block_id;
+    p.out = out;
+    p.plane_stride = batch * part_dim;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool silu = activation == KDA_ACT_SILU;
+    if (l.x_dtype == KDA_DTYPE_F16)
+        dispatch_update<KDA_DTYPE_F16>(p, blocks, silu, s);
+    else if (l.x_dtype == KDA_DTYPE_F32)
+        dispatch_update<KDA_DTYPE_F32>(p, blocks, silu, s);
+    else
+        dispatch_update<KDA_DTYPE_BF16>(p, blocks, silu, s);
+    return record_cuda_error();
+}
+
 }  // namespace
 
 extern "C" {
@@ -800,6 +1001,15 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
     return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
                has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
                false, layout, stream);
+}
+
+kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
+                              int64_t part_dim, const float *weight, const float *bias,
+                              float *conv_states, const int32_t *cache_indices,
+                              int64_t null_block_id, int activation, void *out,
+                              const kda_conv_layout_t *layout, kda_stream_t stream) {
+    return run_update(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
+                      cache_indices, null_block_id, activation, out, layout, stream);
 }
 
 kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, int64_t tokens,

@@ -1,0 +1,101 @@
+"""GPU parity of kda_conv1d_update (one token per sequence) against the oracle
+run with query_start_loc = 0..batch and every has_initial_state set.
+
+Bar as for the packed path: conv states and activation-free outputs
+bit-exact, SiLU outputs within one ulp of the 16-bit types (2^-20 relative
+for fp32)."""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import pins
+import workloads
+from test_general_layout_gpu import _compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    pkg.lib()
+
+
+def _decode_batch(seed, batch, dim, part_dim, row_stride, lines, **kw):
+    b = workloads.make_batch(f"dec{seed}", seed, [1] * batch, dim, part_dim, row_stride, lines,
+                             his_p=1.0, **kw)
+    b.has_initial_state[:] = 1  # the update continues every live sequence
+    return b
+
+
+def _run_update(b, position_major=False, tap_major=False):
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    dev = torch.device("cuda")
+    f32 = b.x_dtype == "f32"
+    x = torch.from_numpy(b.x_buf if f32 else b.x_buf.view(np.int16)).to(dev)
+    out = torch.full((b.dim // b.part_dim, b.tokens, b.part_dim), float("nan") if f32 else -1,
+                     dtype=torch.float32 if f32 else torch.int16, device=dev)
+    if position_major:
+        st = torch.from_numpy(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1))).to(dev)
+        st = st.transpose(1, 2)
+    else:
+        st = torch.from_numpy(b.conv_states).to(dev)
+    w = (torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t() if tap_major
+         else torch.from_numpy(b.weight).to(dev))
+    bias = None if b.bias is None else torch.from_numpy(b.bias).to(dev)
+    ci = torch.from_numpy(b.cache_indices).to(dev)
+    dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
+    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride())
+    esz = 4 if f32 else 2
+    pkg.kda_conv1d_update(x.data_ptr() + esz * b.col_offset, b.row_stride, b.tokens, b.dim,
+                          b.part_dim, w, bias, st, ci, b.null_block_id, b.activation, out, layout)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), st.contiguous().cpu().numpy()
+
+
+CASES = [
+    ("bf16_silu", 501, 300, 256, 128, 264, 8, {}),
+    ("bf16_none", 502, 77, 128, 64, 128, 0, {"activation": 0, "bias_std": None}),
+    ("f16_silu", 503, 129, 192, 64, 200, 8, {"x_dtype": "f16"}),
+    ("f32_none", 504, 64, 128, 128, 132, 4, {"x_dtype": "f32", "activation": 0}),
+    ("bf16_k4", 505, 90, 128, 64, 128, 0, {"state_width": 4}),
+    ("f16_k6_silu", 506, 33, 256, 256, 256, 0, {"x_dtype": "f16", "state_width": 6}),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("position_major", [False, True], ids=["dense", "position_major"])
+@pytest.mark.parametrize("tap_major", [False, True], ids=["w_channel_major", "w_tap_major"])
+def test_update_matches_oracle(case, position_major, tap_major):
+    name, seed, batch, dim, part_dim, row_stride, col_offset, extra = case
+    b = _decode_batch(seed, batch, dim, part_dim, row_stride, 2 * batch, col_offset=col_offset,
+                      null_count=3, **extra)
+    st = b.conv_states.copy()
+    ref = pins.run_oracle_ex(b, states=st)
+    got, got_st = _run_update(b, position_major, tap_major)
+    assert np.array_equal(got_st.view(np.uint32), st.view(np.uint32))
+    _compare(b, got, ref["out"])
+
+
+def test_update_decode_workload_and_repeated_steps():
+    """The 1024-sequence decode batch, three steps in a row: each step's state
+    feeds the next, as in generation."""
+    b = workloads.decode()
+    b.cache_indices[::97] = b.null_block_id
+    dev_states = None
+    st = b.conv_states.copy()
+    for step in range(3):
+        c = b.copy()
+        c.x_buf = np.roll(b.x_buf, step, axis=1).copy()  # a different token row per step
+        c.conv_states = st.copy() if dev_states is None else dev_states
+        ref = pins.run_oracle_ex(c, states=st)
+        got, dev_states = _run_update(c)
+        assert np.array_equal(dev_states.view(np.uint32), st.view(np.uint32)), step
+        _compare(c, got, ref["out"])

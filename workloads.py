@@ -22,6 +22,8 @@ token prefill chunks, row-strided bf16 slices of a wider projection):
                 6400, 2048 cache lines, his ~ Bernoulli(0.8), SiLU, seed 3
   large_nobias  4 x 8192 tokens, dim 3264 = 3 x 1088, dense rows, x ~ N(0, 2^2),
                 weight U(-1, 1), no bias, no activation, seed 4
+  decode        1024 sequences of 1 token (a decode step), dim 4608, row stride
+                6400, 2048 cache lines, every sequence with an initial state, seed 5
 """
 
 from __future__ import annotations
@@ -173,12 +175,18 @@ def large_nobias() -> Batch:
                       w_range=1.0, bias_std=None, activation=0, his=[1, 0, 1, 0])
 
 
+def decode() -> Batch:
+    """1024 sequences of one token each (a decode step), 2048 cache lines."""
+    return make_batch("decode", 5, [1] * 1024, 4608, 1536, 6400, 2048, his_p=1.0)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "varlen": varlen,
     "long16k": long16k,
     "short_decode": short_decode,
     "large_nobias": large_nobias,
+    "decode": decode,
 }
 
 
