@@ -231,18 +231,27 @@ def call(pkg, b: workloads.Batch, s: dict, stream) -> None:
 
 def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, dist: Dist,
                 dev, flush: torch.Tensor | None = None) -> dict:
-    """W untimed steps, then exactly K timed steps between barrier+sync pairs.
-    Each step uses the next input/output set; every launch is bracketed by
-    events on the launching stream.  With `flush` (small workloads whose sets
-    fit in L2), the buffer is rewritten before each step, outside the events."""
+    """W untimed steps, then exactly K timed steps between barrier+sync pairs,
+    each step on the next input/output set, on one stream.
+
+    Without `flush` the K launches run back to back between two region events
+    (as a model's layers would issue them); the average launch duration is the
+    region over K.  With `flush` (batches too small to rotate out of L2) a
+    buffer larger than L2 is rewritten before each step and each launch is
+    bracketed by its own events, which then give the step time.  Afterwards,
+    outside the timed region, up to 200 more launches with per-launch events
+    give the isolated launch time."""
     stream = torch.cuda.Stream(device=dev)
     for i in range(warmup):
         call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
     torch.cuda.synchronize(dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    region0 = torch.cuda.Event(enable_timing=True)
-    region1 = torch.cuda.Event(enable_timing=True)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    starts = [ev() for _ in range(steps)] if flush is not None else []
+    ends = [ev() for _ in range(steps)] if flush is not None else []
+    region0, region1 = ev(), ev()
     dist.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(dev.index or 0) as clocks:
@@ -251,14 +260,32 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
             if flush is not None:
                 with torch.cuda.stream(stream):
                     flush.fill_(i & 0xFF)
-            starts[i].record(stream)
+                starts[i].record(stream)
             call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
-            ends[i].record(stream)
+            if flush is not None:
+                ends[i].record(stream)
         region1.record(stream)
         torch.cuda.synchronize(dev)
     dist.barrier()
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return {"region_ms": region0.elapsed_time(region1), "kernel_ms": kernel_ms,
+    region_ms = region0.elapsed_time(region1)
+    if flush is not None:
+        launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        step_ms = sum(launch_ms)
+    else:
+        step_ms = region_ms
+    # isolated launches, for reference (events between launches prevent overlap)
+    n_iso = min(200, max(steps, 1))
+    iso = [(ev(), ev()) for _ in range(n_iso)]
+    for i, (s0, s1) in enumerate(iso):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.fill_(i & 0xFF)
+        s0.record(stream)
+        call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+        s1.record(stream)
+    torch.cuda.synchronize(dev)
+    iso_ms = [s0.elapsed_time(s1) for s0, s1 in iso]
+    return {"step_ms_total": step_ms, "region_ms": region_ms, "iso_ms": iso_ms,
             "clocks": clocks.summary()}
 
 
@@ -408,11 +435,8 @@ def run_ours(args) -> None:
     torch.cuda.synchronize(dev)
 
     t = time_device(pkg, b, sets, args.steps, args.warmup, dist, dev, flush)
-    kern_mean = statistics.fmean(t["kernel_ms"])
-    # With flushes in the timed region, the step time is the launches' own time.
-    region = t["region_ms"] if flush is None else sum(t["kernel_ms"])
-    ms_per_step, value = aggregate(dist, world, nbytes, region, args.steps, dev)
-    kern_mean_max = dist.max(kern_mean, dev)
+    ms_per_step, value = aggregate(dist, world, nbytes, t["step_ms_total"], args.steps, dev)
+    iso_median = dist.max(statistics.median(t["iso_ms"]), dev)
 
     e2e = time_e2e(pkg, b, args.e2e_steps, dev)
     e2e_ms = dist.max(e2e["ms"], dev)
@@ -422,15 +446,18 @@ def run_ours(args) -> None:
         return
 
     peak, peak_kind = measured_peaks()
-    achieved = nbytes / (kern_mean_max * 1e-3) / 1e9
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9
     extra = {
         "vs_baseline": round(value / world / PAGE_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(), "peak_source": peak_kind,
-                     "kernel": "kda_packed_conv1d_kernel",
-                     "kernel_us_mean": round(kern_mean_max * 1e3, 3),
-                     "kernel_us_median": round(statistics.median(t["kernel_ms"]) * 1e3, 3)},
+                     "kernel": ("kda_conv1d_update_kernel" if ENTRY == "update"
+                                else "kda_packed_conv1d_kernel"),
+                     "launch_us_mean": round(ms_per_step * 1e3, 3),
+                     "launch_us_isolated_median": round(iso_median * 1e3, 3),
+                     "timing": ("back-to-back launches, region events / K" if flush is None else
+                                "per-launch events after an L2 flush")},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": round(e2e_ms, 4),

@@ -65,6 +65,10 @@
 #define KDA_STORE_CS 1  // 1: plane stores use the streaming (evict-first) cache hint
 #endif
 
+#ifndef KDA_PDL
+#define KDA_PDL 1  // 1: launch as a programmatic dependent of the preceding kernel (launch_kernel)
+#endif
+
 #if KDA_LOAD_L2_256
 #define KDA_LD_X "ld.global.nc.L1::no_allocate.L2::256B"
 #else
@@ -298,6 +302,13 @@ __host__ __device__ constexpr int min_blocks() {
 template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
 __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
     kda_packed_conv1d_kernel(const Params p) {
+#if KDA_PDL
+    // Launched as a programmatic dependent: wait until the preceding grid in
+    // the stream has completed and its writes are visible (the same order a
+    // plain launch gives), and let the next grid be scheduled meanwhile.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+#endif
     constexpr int W = row_words<VEC, kDtype>();
     // x and out are addressed in elements of their storage type
     using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
@@ -546,6 +557,10 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 
 template <int VEC, int kDtype, bool kGeneral, bool kSilu, bool kBias>
 __global__ void __launch_bounds__(256, 4) kda_conv1d_update_kernel(const Params p) {
+#if KDA_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+#endif
     constexpr int W = row_words<VEC, kDtype>();
     using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
     const int64_t nvec = p.dim / VEC;
@@ -670,6 +685,7 @@ __global__ void __launch_bounds__(256, 4) kda_conv1d_update_kernel(const Params 
 // ---------------------------------------------------------------------------
 
 thread_local char g_last_error[256] = "";
+thread_local cudaError_t g_launch_status = cudaSuccess;  // of the last cudaLaunchKernelEx
 
 constexpr int kVec = KDA_VEC;                 // channels per thread
 constexpr int kQueue = KDA_QUEUE;             // rows in flight per thread
@@ -796,10 +812,38 @@ int current_sms() {
     return cache[dev];
 }
 
+// Launches a conv kernel.  With KDA_PDL the launch carries the programmatic
+// stream serialization attribute: the grid may be scheduled while the
+// preceding kernel in the stream drains (when that kernel signals
+// griddepcontrol.launch_dependents, as these kernels do), and the kernel's
+// first instruction, griddepcontrol.wait, holds every thread until that
+// kernel has completed and its writes are visible.  Stream order is exactly
+// that of a plain launch; what overlaps is the launch and the block
+// scheduling, not any memory access.  After any other kind of predecessor
+// the launch behaves as a plain one.
+void launch_kernel(void (*kernel)(Params), unsigned blocks, unsigned threads, const Params &p,
+                   cudaStream_t stream) {
+#if KDA_PDL
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    g_launch_status = cudaLaunchKernelEx(&cfg, kernel, p);
+#else
+    kernel<<<blocks, threads, 0, stream>>>(p);
+#endif
+}
+
 template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
 void launch(const Params &p, const Shape &sh, cudaStream_t stream) {
-    kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias>
-        <<<(unsigned)sh.ctas, sh.threads, 0, stream>>>(p);
+    launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias>,
+                  (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
 }
 
 template <int kDtype, bool kGeneral>
@@ -826,7 +870,9 @@ void dispatch(const Params &p, const Shape &sh, bool silu, cudaStream_t s) {
 }
 
 kda_status_t record_cuda_error() {
-    const cudaError_t err = cudaGetLastError();
+    cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) err = g_launch_status;
+    g_launch_status = cudaSuccess;
     if (err != cudaSuccess) {
         snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
                  cudaGetErrorString(err));
@@ -904,8 +950,8 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
 
 template <int kDtype, bool kGeneral, bool kSilu, bool kBias>
 void launch_update(const Params &p, int64_t blocks, cudaStream_t stream) {
-    kda_conv1d_update_kernel<kVec, kDtype, kGeneral, kSilu, kBias>
-        <<<(unsigned)blocks, 256, 0, stream>>>(p);
+    launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kGeneral, kSilu, kBias>,
+                  (unsigned)blocks, 256, p, stream);
 }
 
 template <int kDtype, bool kGeneral>
