@@ -13,6 +13,7 @@ import torch
 
 import pins
 import workloads
+from gpu_helpers import ulp_diff
 from test_general_layout_gpu import _compare
 
 pytestmark = pytest.mark.gpu
@@ -99,3 +100,58 @@ def test_update_decode_workload_and_repeated_steps():
         got, dev_states = _run_update(c)
         assert np.array_equal(dev_states.view(np.uint32), st.view(np.uint32)), step
         _compare(c, got, ref["out"])
+
+
+def test_back_to_back_chain_on_one_state_buffer():
+    """Calls that read the conv state the previous call wrote, issued back to
+    back on one stream with nothing in between (all inputs uploaded and all
+    outputs allocated first), so consecutive launches are adjacent and overlap
+    their scheduling while each waits for its predecessor: a packed prefill,
+    12 decode updates, another packed call; against the oracle in the same
+    order."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    dev = torch.device("cuda")
+    lines, dim, part = 40, 256, 128
+    pre = workloads.make_batch("chain_pre", 601, [37, 5, 90, 1], dim, part, 264, lines,
+                               col_offset=8, his_p=0.5)
+    calls = [("packed", pre)]
+    for step in range(12):
+        d = workloads.make_batch(f"chain_dec{step}", 610 + step, [1] * 4, dim, part, 264, lines,
+                                 col_offset=8)
+        calls.append(("update", d))
+    calls.append(("packed", workloads.make_batch("chain_post", 630, [3, 20, 2, 9], dim, part,
+                                                 264, lines, col_offset=8)))
+    for _, b in calls[1:]:
+        b.weight, b.bias = pre.weight, pre.bias
+        b.cache_indices = pre.cache_indices.copy()
+        b.has_initial_state[:] = 1
+
+    dev_st = torch.from_numpy(pre.conv_states).to(dev)
+    w = torch.from_numpy(pre.weight).to(dev)
+    bias = torch.from_numpy(pre.bias).to(dev)
+    staged = []
+    for kind, b in calls:
+        staged.append(dict(
+            x=torch.from_numpy(b.x_buf.view(np.int16)).to(dev),
+            out=torch.full((dim // part, b.tokens, part), -1, dtype=torch.int16, device=dev),
+            meta=[torch.from_numpy(a).to(dev) for a in
+                  (b.cache_indices, b.has_initial_state, b.query_start_loc)]))
+    torch.cuda.synchronize()
+    for (kind, b), sd in zip(calls, staged):  # back to back
+        xp = sd["x"].data_ptr() + 2 * b.col_offset
+        ci, his, qsl = sd["meta"]
+        if kind == "packed":
+            pkg.kda_packed_conv1d(xp, b.row_stride, b.tokens, dim, part, w, bias, dev_st, ci,
+                                  his, qsl, b.num_seqs, b.null_block_id, b.activation, sd["out"])
+        else:
+            pkg.kda_conv1d_update(xp, b.row_stride, b.tokens, dim, part, w, bias, dev_st, ci,
+                                  b.null_block_id, b.activation, sd["out"])
+    torch.cuda.synchronize()
+
+    st_ref = pre.conv_states.copy()
+    for (kind, b), sd in zip(calls, staged):
+        want = pins.run_oracle_ex(b, states=st_ref)["out"]
+        d = ulp_diff(sd["out"].cpu().numpy().view(np.uint16), want)
+        assert d.max() <= 1, kind
+    assert np.array_equal(dev_st.cpu().numpy().view(np.uint32), st_ref.view(np.uint32))
