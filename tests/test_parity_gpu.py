@@ -211,3 +211,18 @@ def test_nonzero_stream_and_null_block_none():
     ref, ref_states = oracle_run(b)
     assert_states_equal(d.states(), ref_states)
     assert_outputs_match(out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"], 1)
+
+
+def test_many_sequences_four_search_levels():
+    """40,000 sequences (lengths 0..5, some null blocks): the program search
+    needs four radix-32 levels (32^3 < 40,000)."""
+    rng = np.random.default_rng(7)
+    lengths = rng.integers(0, 6, size=40000).tolist()
+    b = workloads.make_batch("many", 701, lengths, 64, 64, 64, 40010, his_p=0.5,
+                             null_count=500)
+    ref, ref_states = oracle_run(b)
+    d = DeviceBatch(b)
+    d.run()
+    torch.cuda.synchronize()
+    assert_states_equal(d.states(), ref_states)
+    assert_outputs_match(d.out_bits(), ref["out"], b.activation)
