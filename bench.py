@@ -47,7 +47,7 @@ UNIT = "GB/s"
 PAGE_GBS = 4800.0  # the page's ~4.8 TB/s for its packed kernel at 2K-16K x 3x1536 on GB300
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRC = os.path.join(ROOT, "linear_attention_prefill_varlen_gb300", "csrc", "kda_conv.cu")
-PROFILE = os.path.join(ROOT, "profiles", "kda_packed_conv1d_long16k.md")
+PROFILES = os.path.join(ROOT, "profiles")
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -81,11 +81,17 @@ def kernel_sha() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic() -> int | None:
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
-    the current kernel source (its sha line matches)."""
+def profile_path(entry: str, workload: str) -> str:
+    kernel = "kda_conv1d_update" if entry == "update" else "kda_packed_conv1d"
+    return os.path.join(PROFILES, f"{kernel}_{workload}.md")
+
+
+def recorded_traffic(entry: str, workload: str) -> int | None:
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel on
+    this workload, if there is one and it was taken on the current kernel
+    source (its sha line matches)."""
     try:
-        text = open(PROFILE).read()
+        text = open(profile_path(entry, workload)).read()
     except OSError:
         return None
     sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
@@ -471,7 +477,7 @@ def run_ours(args) -> None:
         "vs_baseline": round(value / world / PAGE_GBS, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(), "peak_source": peak_kind,
+                     "traffic": recorded_traffic(ENTRY, b.name), "peak_source": peak_kind,
                      "kernel": ("kda_conv1d_update_kernel" if ENTRY == "update"
                                 else "kda_packed_conv1d_kernel"),
                      "launch_us_mean": round(ms_per_step * 1e3, 3),

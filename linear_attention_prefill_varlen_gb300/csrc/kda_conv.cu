@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 // ---------------------------------------------------------------------------
 
 template <int VEC, int kDtype, bool kGeneral, bool kSilu, bool kBias>
-__global__ void __launch_bounds__(256, 4) kda_conv1d_update_kernel(const Params p) {
+__global__ void __launch_bounds__(256, kGeneral ? 2 : 4) kda_conv1d_update_kernel(const Params p) {
 #if KDA_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
