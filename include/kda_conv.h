@@ -37,7 +37,10 @@
  * stated; the conv calls are asynchronous on the given stream, allocate
  * nothing, never synchronise, and launch a grid that depends only on the
  * scalar arguments (so a captured launch replays correctly for new metadata
- * values of the same tokens / num_seqs).
+ * values of the same tokens / num_seqs). The conv kernels are launched as
+ * programmatic dependents of the preceding kernel in the stream: they may be
+ * scheduled while it drains, but every thread first waits until it has
+ * completed and its writes are visible, so ordering is that of a plain launch.
  */
 #ifndef KDA_CONV_H_
 #define KDA_CONV_H_
