@@ -226,3 +226,29 @@ def test_many_sequences_four_search_levels():
     torch.cuda.synchronize()
     assert_states_equal(d.states(), ref_states)
     assert_outputs_match(d.out_bits(), ref["out"], b.activation)
+
+
+def test_offsets_beyond_32_bits():
+    """40M token rows x 64 channels: the output plane offset and the x row
+    offset of the last rows exceed 2^31 elements.  One 100-token sequence
+    at the very end (qsl[0] = 40M - 150, so thousands of leading programs own
+    no rows and exit after the search); only its rows are compared."""
+    T, D, start, L = 40_000_000, 64, 40_000_000 - 150, 100
+    rng = np.random.default_rng(11)
+    x_buf = np.zeros((T, D), dtype=np.uint16)
+    vals = torch.from_numpy(rng.standard_normal((L, D)).astype(np.float32))
+    x_buf[start:start + L] = vals.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    b = workloads.Batch("offsets", x_buf, 0, D, D,
+                        rng.uniform(-0.5, 0.5, (D, 4)).astype(np.float32),
+                        (rng.standard_normal(D) * 0.1).astype(np.float32),
+                        rng.standard_normal((2, D, 3)).astype(np.float32),
+                        np.array([1], dtype=np.int32), np.array([1], dtype=np.uint8),
+                        np.array([start, start + L], dtype=np.int32), -1, 1, 11)
+    ref, ref_states = oracle_run(b)
+    d = DeviceBatch(b)
+    d.run()
+    torch.cuda.synchronize()
+    assert_states_equal(d.states(), ref_states)
+    got = d.out[:, start - 50:].cpu().numpy().view(np.uint16)
+    assert_outputs_match(got, ref["out"][:, start - 50:], 1)
+    assert (d.out[:, :start].eq(-1)).all().item()  # rows before the sequence untouched

@@ -155,3 +155,44 @@ def test_back_to_back_chain_on_one_state_buffer():
         d = ulp_diff(sd["out"].cpu().numpy().view(np.uint16), want)
         assert d.max() <= 1, kind
     assert np.array_equal(dev_st.cpu().numpy().view(np.uint32), st_ref.view(np.uint32))
+
+
+def test_update_in_cuda_graph_replays_with_new_metadata():
+    """A captured decode update replays correctly after the x rows and cache
+    indices change (same batch size)."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    b1 = _decode_batch(801, 64, 256, 128, 256, 200, null_count=2)
+    b2 = b1.copy()
+    b2.x_buf = np.roll(b1.x_buf, 3, axis=0).copy()
+    b2.cache_indices = np.random.default_rng(3).permutation(200)[:64].astype(np.int32)
+    dev = torch.device("cuda")
+    x = torch.from_numpy(b1.x_buf.view(np.int16)).to(dev)
+    st = torch.from_numpy(b1.conv_states).to(dev)
+    w = torch.from_numpy(b1.weight).to(dev)
+    bias = torch.from_numpy(b1.bias).to(dev)
+    ci = torch.from_numpy(b1.cache_indices).to(dev)
+    out = torch.full((2, 64, 128), -1, dtype=torch.int16, device=dev)
+    stream = torch.cuda.Stream()
+
+    def step(s):
+        pkg.kda_conv1d_update(x, b1.row_stride, 64, 256, 128, w, bias, st, ci, b1.null_block_id,
+                              b1.activation, out, None, s)
+
+    step(stream)  # outside capture: first-use set-up
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step(torch.cuda.current_stream())
+    for b in (b1, b2):
+        x.copy_(torch.from_numpy(b.x_buf.view(np.int16)))
+        st.copy_(torch.from_numpy(b.conv_states))
+        ci.copy_(torch.from_numpy(b.cache_indices))
+        out.fill_(-1)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref_st = b.conv_states.copy()
+        ref = pins.run_oracle_ex(b, states=ref_st)
+        assert np.array_equal(st.cpu().numpy().view(np.uint32), ref_st.view(np.uint32))
+        _compare(b, out.cpu().numpy(), ref["out"])
