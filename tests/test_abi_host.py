@@ -198,3 +198,10 @@ def test_null_layout_is_the_default(kda):
             a["bias"], a["conv_states"], a["cache_indices"], a["has_initial_state"],
             a["query_start_loc"], a["num_seqs"], a["activation"], a["out"])
     assert kda.check_args_ex(*args, None) == kda.check_args(*args) == 3
+
+
+def test_supported_predicate_rejects_host_tensors(kda):
+    x = torch.zeros(8, 128, dtype=torch.bfloat16)
+    w = torch.zeros(128, 4)
+    st = torch.zeros(2, 128, 3)
+    assert not kda.packed_causal_conv1d_supported(x, w, st, 64)
