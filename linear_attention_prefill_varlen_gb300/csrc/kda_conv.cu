@@ -35,6 +35,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kda_conv.h"
@@ -798,18 +799,19 @@ Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
     return sh;
 }
 
-// SM count of the current device, cached per device.
+// SM count of the current device, cached per device (host threads may race to
+// fill an entry; they store the same value).
 int current_sms() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kDefaultSms;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = kDefaultSms;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // Launches a conv kernel.  With KDA_PDL the launch carries the programmatic
