@@ -252,3 +252,27 @@ def test_offsets_beyond_32_bits():
     got = d.out[:, start - 50:].cpu().numpy().view(np.uint16)
     assert_outputs_match(got, ref["out"][:, start - 50:], 1)
     assert (d.out[:, :start].eq(-1)).all().item()  # rows before the sequence untouched
+
+
+@pytest.mark.parametrize("activation,silu", [("silu", True), ("swish", True), (True, True),
+                                             (None, False), ("none", False), (False, False)])
+def test_page_wrapper_activation_names_and_out(activation, silu):
+    """packed_causal_conv1d_fn selects SiLU for "silu", "swish" and True, as the
+    page's wrapper does, and no activation otherwise; a caller-provided `out`
+    receives the result."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    b = pins.small_batch(950, [20, 3, 41], dim=256, part_dim=128, null_count=0, cache_lines=5,
+                         col_offset=0, row_stride=256, activation=1 if silu else 0)
+    d = DeviceBatch(b)
+    x = d.x_buf.view(torch.bfloat16)
+    out = torch.full((2, b.tokens, 128), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    ret = pkg.packed_causal_conv1d_fn(x, d.weight, d.bias, d.conv_states, d.query_start_loc,
+                                      d.cache_indices, d.has_initial_state, b.part_dim,
+                                      activation=activation, null_block_id=-1, out=out)
+    torch.cuda.synchronize()
+    assert ret.data_ptr() == out.data_ptr()
+    ref, ref_states = oracle_run(b)
+    assert_states_equal(d.states(), ref_states)
+    assert_outputs_match(out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"],
+                         b.activation)
