@@ -75,7 +75,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.kda_ref_packed_conv1d_ex.argtypes = [
         P, ctypes.c_int, I64, I64, I64, I64,  # x, dtype, x_row_stride, tokens, dim, part_dim
         P, I64, I64, P,  # weight, w_stride_c, w_stride_j, bias
-        P, I64, I64, I64, I64, I64,  # conv_states, lines, width, strides (line, c, k)
+        P, ctypes.c_int, I64, I64, I64, I64, I64,  # conv_states, state dtype, lines, width, strides
         P, P, P, I64, I64,  # cache_indices, has_initial_state, qsl, num_seqs, null_block_id
         ctypes.c_int, P, P,  # activation, out, preact
     ]
@@ -235,7 +235,8 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
     ``x_buf`` (tokens, row_stride): uint16 bits for bf16 / fp16, float32 for
     fp32; the input is columns [col_offset, col_offset + dim).  ``weight`` is
     a (dim, 4) float32 view with any strides; ``conv_states`` a
-    (lines, dim, K) float32 view with any strides, updated in place.  Returns
+    (lines, dim, K) view with any strides, float32 or uint16 (bf16 bits),
+    updated in place.  Returns
     ``out`` (dim/part_dim, tokens, part_dim) of x's storage type, filled with
     0xFFFF bits (NaN for fp32) where no sequence writes, and optionally
     ``preact``."""
@@ -244,7 +245,8 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
     assert (x_buf.dtype == np.float32) == (dtype == DTYPE_F32)
     tokens, row_stride = x_buf.shape
     assert weight.dtype == np.float32 and weight.shape == (dim, 4)
-    assert conv_states.dtype == np.float32 and conv_states.ndim == 3
+    assert conv_states.dtype in (np.float32, np.uint16) and conv_states.ndim == 3
+    state_dtype = DTYPE_F32 if conv_states.dtype == np.float32 else DTYPE_BF16
     assert conv_states.shape[1] == dim
     ws = _elem_strides(weight)
     ss = _elem_strides(conv_states)
@@ -261,7 +263,8 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
     rc = lib.kda_ref_packed_conv1d_ex(
         x_buf.ctypes.data + x_buf.itemsize * col_offset, dtype, row_stride, tokens, dim, part_dim,
         weight.ctypes.data, ws[0], ws[1], _ptr(bias),
-        conv_states.ctypes.data, conv_states.shape[0], conv_states.shape[2], ss[0], ss[1], ss[2],
+        conv_states.ctypes.data, state_dtype, conv_states.shape[0], conv_states.shape[2],
+        ss[0], ss[1], ss[2],
         _ptr(ci), _ptr(his), _ptr(qsl), qsl.size - 1, null_block_id, activation,
         out.ctypes.data, _ptr(preact))
     if rc != REF_OK:

@@ -313,12 +313,15 @@ static void ref_store(void *out, int dtype, int64_t i, float y) {
  *   conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k].
  *   The taps read its last 3 positions; afterwards the line holds the last K
  *   rows of [old state (or zeros) ; the sequence's rows].
+ *   The state is stored as state_dtype: fp32, or bf16 (read exactly, written
+ *   rounded to nearest even; with bf16 x the stored rows are exact).
  * With dtype bf16, K = 3 and contiguous strides this is kda_ref_packed_conv1d.
  */
 int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int64_t tokens,
                              int64_t dim, int64_t part_dim, const float *weight,
                              int64_t w_stride_c, int64_t w_stride_j, const float *bias,
-                             float *conv_states, int64_t cache_lines, int64_t state_width,
+                             void *conv_states, int state_dtype, int64_t cache_lines,
+                             int64_t state_width,
                              int64_t s_stride_line, int64_t s_stride_c, int64_t s_stride_k,
                              const int32_t *cache_indices, const uint8_t *has_initial_state,
                              const int32_t *query_start_loc, int64_t num_seqs,
@@ -330,6 +333,7 @@ int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int
     if (dtype != REF_DTYPE_BF16 && dtype != REF_DTYPE_F16 && dtype != REF_DTYPE_F32)
         return REF_BAD_SHAPE;
     if (state_width < 3 || state_width > 64) return REF_BAD_SHAPE;
+    if (state_dtype != REF_DTYPE_F32 && state_dtype != REF_DTYPE_BF16) return REF_BAD_SHAPE;
     if (tokens == 0 || num_seqs == 0) return REF_OK;
     int rc = kda_ref_check_metadata(tokens, cache_lines, cache_indices, query_start_loc, num_seqs,
                                     null_block_id, &bad);
@@ -347,7 +351,8 @@ int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int
         for (int64_t c = 0; c < dim; ++c) {
             float h[64];
             for (int64_t k = 0; k < K; ++k)
-                h[k] = read_state ? conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k]
+                h[k] = read_state ? ref_load(conv_states, state_dtype,
+                                             line * s_stride_line + c * s_stride_c + k * s_stride_k)
                                   : 0.0f;
             int64_t plane = c / part_dim;
             int64_t col = c % part_dim;
@@ -372,7 +377,8 @@ int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int
                     ns[k] = (r >= 0) ? ref_load(x, dtype, (a + r) * x_row_stride + c) : h[k + len];
                 }
                 for (int64_t k = 0; k < K; ++k)
-                    conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k] = ns[k];
+                    ref_store(conv_states, state_dtype,
+                              line * s_stride_line + c * s_stride_c + k * s_stride_k, ns[k]);
             }
         }
     }

@@ -690,3 +690,36 @@ def pin_ex_strides(lib) -> None:
 
 ALL_PINS += [pin_f16_widen, pin_f16_rne, pin_ex_matches_basic, pin_ex_typed_exact,
              pin_ex_state_width, pin_ex_strides]
+
+
+def pin_ex_bf16_state(lib) -> None:
+    """A bf16 conv state: with bf16 x it holds exactly the values an fp32
+    state would (the stored rows are input rows), so outputs and states match
+    the fp32-state run bit for bit; with fp32 x the stored rows are torch's
+    nearest-even rounding of the last K rows of [old line ; x rows]."""
+    for K in (3, 4):
+        b = workloads.make_batch(f"bst{K}", 161 + K, [1, 2, 9, 30], 128, 64, 136, 7,
+                                 col_offset=8, his_p=0.6, null_count=1, state_width=K)
+        b.conv_states = torch_bf16_to_f32(torch_f32_to_bf16(b.conv_states))  # bf16 values
+        st32 = b.conv_states.copy()
+        st16 = torch_f32_to_bf16(b.conv_states)
+        r32 = run_oracle_ex(b, lib, states=st32)
+        r16 = run_oracle_ex(b, lib, states=st16)
+        assert np.array_equal(r32["out"], r16["out"])
+        assert np.array_equal(torch_bf16_to_f32(st16).view(np.uint32), st32.view(np.uint32))
+    b = workloads.make_batch("bst_f32x", 170, [1, 2, 5, 11], 64, 64, 68, 6, col_offset=4,
+                             his_p=0.7, null_count=1, x_dtype="f32", state_width=4)
+    st16 = torch_f32_to_bf16(b.conv_states)
+    old = torch_bf16_to_f32(st16)
+    run_oracle_ex(b, lib, states=st16)
+    for s in range(b.num_seqs):
+        line = int(b.cache_indices[s])
+        if line == b.null_block_id:
+            continue
+        a, e = int(b.query_start_loc[s]), int(b.query_start_loc[s + 1])
+        prev = old[line] if b.has_initial_state[s] else np.zeros_like(old[line])
+        want = np.concatenate([prev.T, x_as_f32(b, slice(a, e))])[-4:].T
+        assert np.array_equal(st16[line], torch_f32_to_bf16(np.ascontiguousarray(want))), s
+
+
+ALL_PINS.append(pin_ex_bf16_state)

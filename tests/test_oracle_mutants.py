@@ -48,6 +48,9 @@ MUTANTS = [
     ("f16_no_subnormals", "int q = (e >= -14) ? e - 10 : -24;", "int q = e - 10;"),
     ("f16_widen_subnormal", "float v = ldexpf((float)frac, -24);",
      "float v = ldexpf((float)frac, -25);"),
+    # stays in bounds: bf16 stores into an fp32 state only touch the array's own bytes
+    ("state_stored_as_bf16_always", "ref_store(conv_states, state_dtype,",
+     "ref_store(conv_states, REF_DTYPE_BF16,"),
 ]
 
 
