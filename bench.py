@@ -45,6 +45,7 @@ import workloads  # noqa: E402
 METRIC = "HBM GB/s (read+write) & % of GB300 peak; packed QKV conv 16K x 3x1536 bf16"
 UNIT = "GB/s"
 PAGE_GBS = 4800.0  # the page's ~4.8 TB/s for its packed kernel at 2K-16K x 3x1536 on GB300
+PAGE_WORKLOADS = ("long16k", "varlen")  # the workloads inside that range
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SRC = os.path.join(ROOT, "linear_attention_prefill_varlen_gb300", "csrc", "kda_conv.cu")
 PROFILES = os.path.join(ROOT, "profiles")
@@ -205,13 +206,17 @@ def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
     """Device copies of one batch.  dense_x stores x as (tokens, dim) contiguous."""
     x_np = b.x_buf[:, b.col_offset:b.col_offset + b.dim] if dense_x else b.x_buf
     x = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).to(dev)
+    if b.conv_states.dtype == np.uint16:  # bf16 bits
+        states = torch.from_numpy(b.conv_states.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        states = torch.from_numpy(b.conv_states).to(dev)
     return {
         "x": x,
         "x_ptr": x.data_ptr() + (0 if dense_x else 2 * b.col_offset),
         "x_row_stride": b.dim if dense_x else b.row_stride,
         "weight": torch.from_numpy(b.weight).to(dev),
         "bias": None if b.bias is None else torch.from_numpy(b.bias).to(dev),
-        "conv_states": torch.from_numpy(b.conv_states).to(dev),
+        "conv_states": states,
         "cache_indices": torch.from_numpy(b.cache_indices).to(dev),
         "has_initial_state": torch.from_numpy(b.has_initial_state).to(dev),
         "query_start_loc": torch.from_numpy(b.query_start_loc).to(dev),
@@ -223,11 +228,27 @@ def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
 ENTRY = "packed"
 
 
+def state_layout(pkg, states: torch.Tensor):
+    """None (the default layout) for an fp32 state, else a bf16-state layout."""
+    if states.dtype != torch.bfloat16:
+        return None
+    return pkg.make_layout(pkg.KDA_DTYPE_BF16, states.size(2), states.stride(), (4, 1),
+                           pkg.KDA_DTYPE_BF16)
+
+
 def call(pkg, b: workloads.Batch, s: dict, stream) -> None:
+    if "layout" not in s:
+        s["layout"] = state_layout(pkg, s["conv_states"])
     if ENTRY == "update":
         pkg.kda_conv1d_update(s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim,
                               s["weight"], s["bias"], s["conv_states"], s["cache_indices"],
-                              b.null_block_id, b.activation, s["out"], None, stream)
+                              b.null_block_id, b.activation, s["out"], s["layout"], stream)
+        return
+    if s["layout"] is not None:
+        pkg.kda_packed_conv1d_ex(s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim,
+                                 s["weight"], s["bias"], s["conv_states"], s["cache_indices"],
+                                 s["has_initial_state"], s["query_start_loc"], b.num_seqs,
+                                 b.null_block_id, b.activation, s["out"], s["layout"], stream)
         return
     pkg.kda_packed_conv1d(s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim,
                           s["weight"], s["bias"], s["conv_states"], s["cache_indices"],
@@ -361,9 +382,14 @@ def oracle_sample(b: workloads.Batch, seconds: float, max_reps: int = 50) -> dic
     while reps < max_reps and (reps == 0 or t_total < seconds):
         st = b.conv_states.copy()
         t = time.perf_counter()
-        oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
-                             b.cache_indices, b.has_initial_state, b.query_start_loc,
-                             b.null_block_id, b.activation)
+        if st.dtype == np.uint16:  # bf16 state: the general-layout oracle
+            oracle.packed_conv1d_ex(b.x_buf, oracle.DTYPE_BF16, b.col_offset, b.dim, b.part_dim,
+                                    b.weight, b.bias, st, b.cache_indices, b.has_initial_state,
+                                    b.query_start_loc, b.null_block_id, b.activation)
+        else:
+            oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
+                                 b.cache_indices, b.has_initial_state, b.query_start_loc,
+                                 b.null_block_id, b.activation)
         t_total += time.perf_counter() - t
         reps += 1
     nbytes = workloads.algorithmic_bytes(b)
@@ -391,7 +417,8 @@ def base_line(args, world: int, value: float, ms: float, b: workloads.Batch, ext
             "workload": b.name, "tokens": b.tokens, "num_seqs": b.num_seqs, "dim": b.dim,
             "part_dim": b.part_dim, "x_row_stride": b.row_stride,
             "activation": "silu" if b.activation else "none", "bias": b.bias is not None,
-            "storage": "x/out bf16, weight/bias/conv_state fp32",
+            "storage": ("x/out bf16, weight/bias fp32, conv_state "
+                        + ("bf16" if b.conv_states.dtype == np.uint16 else "fp32")),
             "bytes_per_step_per_gpu": workloads.algorithmic_bytes(b),
             "parallelism": f"replicas x{world}",
         },
@@ -474,7 +501,8 @@ def run_ours(args) -> None:
     peak, peak_kind = measured_peaks()
     achieved = nbytes / (ms_per_step * 1e-3) / 1e9
     extra = {
-        "vs_baseline": round(value / world / PAGE_GBS, 4),
+        "vs_baseline": (round(value / world / PAGE_GBS, 4)
+                        if ENTRY == "packed" and b.name in PAGE_WORKLOADS else None),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(ENTRY, b.name), "peak_source": peak_kind,

@@ -65,14 +65,15 @@ typedef enum {
 
 typedef enum { KDA_ACT_NONE = 0, KDA_ACT_SILU = 1 } kda_activation_t;
 
-/* Storage type of x and out (kda_packed_conv1d_ex). */
+/* Storage type of x and out, and of the conv state (kda_conv_layout_t). */
 typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F16 = 1, KDA_DTYPE_F32 = 2 } kda_dtype_t;
 
 /*
  * The general layout of kda_packed_conv1d_ex, after packed_causal_conv1d_supported
  * on the kda_conv page: x may be bf16, fp16 or fp32 (out has x's type, as
- * packed_causal_conv1d_fn returns x.dtype), the FP32 weight and conv state are
- * passed with their strides, and the conv state may be wider than 3.
+ * packed_causal_conv1d_fn returns x.dtype), the FP32 weight and the conv state are
+ * passed with their strides, and the conv state may be wider than 3 or stored
+ * as bf16.
  *   x_dtype        kda_dtype_t of x and out.
  *   state_width    K = conv_states size(2), 3..64. A line holds the K most recent
  *                  rows (position K-1 the newest); the taps read positions K-3..K-1;
@@ -81,12 +82,23 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F16 = 1, KDA_DTYPE_F32 = 2 } kda_dt
  *   state_stride   element strides of conv_states: line, channel, position.
  *   weight_stride  element strides of weight: channel, tap (4, 1 is channel-major;
  *                  1, dim is the tap-major layout of a width-major weight copy).
+ *   state_dtype    KDA_DTYPE_F32 or KDA_DTYPE_BF16 (any other value is
+ *                  KDA_ERR_INVALID_ARG); set it explicitly: a zero-filled struct
+ *                  means bf16. A bf16 state is read exactly (a bf16 is an fp32
+ *                  value) and each value written to it is the FP32 value rounded
+ *                  to nearest even; the accumulation stays FP32 either way. The
+ *                  kda_conv page keeps the state in FP32; the kda_decode page's
+ *                  fused decode kernel (is_fused_kda_decode_supported) takes a
+ *                  bf16 conv state only. bf16 halves a decode step's state traffic.
+ *   reserved       must be 0.
  */
 typedef struct kda_conv_layout {
     int32_t x_dtype;
     int32_t state_width;
     int64_t state_stride[3];
     int64_t weight_stride[2];
+    int32_t state_dtype;
+    int32_t reserved;
 } kda_conv_layout_t;
 
 /*
@@ -131,16 +143,18 @@ kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t toke
 
 /*
  * kda_packed_conv1d_ex -- kda_packed_conv1d with the general layout above; layout
- * NULL means bf16, width 3 and contiguous strides (kda_packed_conv1d itself).
- * Rounding of out: bf16 and fp16 to nearest even, fp32 none. Alignment: x and out
- * 16-byte aligned and x_row_stride a multiple of 16 bytes (8 elements of bf16 /
- * fp16, 4 of fp32); weight 16-byte aligned when its strides are (4, 1), else
- * 4-byte; conv_states 16-byte aligned when it is width 3 and contiguous, else
- * 4-byte; bias 16-byte aligned. Everything else as for kda_packed_conv1d.
+ * NULL means bf16 x, an fp32 state of width 3 and contiguous strides
+ * (kda_packed_conv1d itself). conv_states points to elements of the layout's
+ * state_dtype. Rounding of out: bf16 and fp16 to nearest even, fp32 none.
+ * Alignment: x and out 16-byte aligned and x_row_stride a multiple of 16 bytes
+ * (8 elements of bf16 / fp16, 4 of fp32); weight 16-byte aligned when its strides
+ * are (4, 1), else 4-byte; conv_states 16-byte aligned when it is width 3 and
+ * contiguous, else aligned to its element; bias 16-byte aligned. Everything else
+ * as for kda_packed_conv1d.
  */
 kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t tokens,
                                   int64_t dim, int64_t part_dim, const float *weight,
-                                  const float *bias, float *conv_states,
+                                  const float *bias, void *conv_states,
                                   const int32_t *cache_indices, const uint8_t *has_initial_state,
                                   const int32_t *query_start_loc, int64_t num_seqs,
                                   int64_t null_block_id, int activation, void *out,
@@ -156,13 +170,14 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
  * dropped, x appended). A token whose cache index is null_block_id is computed
  * with a zero history and its line is not touched. The decode-step counterpart of
  * the conv update the kda_decode page's fused decode kernel performs. Layout as
- * for kda_packed_conv1d_ex (NULL: bf16, width 3, contiguous). Cache indices must
+ * for kda_packed_conv1d_ex (NULL: bf16 x, fp32 state, width 3, contiguous); with a
+ * bf16 state the line is 6 bytes per channel instead of 12. Cache indices must
  * be distinct (or null); out must not overlap x or conv_states. Asynchronous on
  * `stream`; allocates nothing.
  */
 kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
                               int64_t part_dim, const float *weight, const float *bias,
-                              float *conv_states, const int32_t *cache_indices,
+                              void *conv_states, const int32_t *cache_indices,
                               int64_t null_block_id, int activation, void *out,
                               const kda_conv_layout_t *layout, kda_stream_t stream);
 
@@ -198,7 +213,7 @@ kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, i
  * kda_packed_conv1d_ex (as kda_packed_conv1d_check_args, with a layout). */
 kda_status_t kda_packed_conv1d_ex_check_args(
     const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
-    const float *weight, const float *bias, const float *conv_states,
+    const float *weight, const float *bias, const void *conv_states,
     const int32_t *cache_indices, const uint8_t *has_initial_state,
     const int32_t *query_start_loc, int64_t num_seqs, int activation, const void *out,
     const kda_conv_layout_t *layout);

@@ -35,15 +35,18 @@ class KdaError(RuntimeError):
 
 
 class KdaConvLayout(ctypes.Structure):
-    """kda_conv_layout_t: x/out dtype, conv-state width and element strides."""
+    """kda_conv_layout_t: x/out dtype, conv-state width, element strides and
+    conv-state dtype."""
 
     _fields_ = [("x_dtype", ctypes.c_int32), ("state_width", ctypes.c_int32),
-                ("state_stride", ctypes.c_int64 * 3), ("weight_stride", ctypes.c_int64 * 2)]
+                ("state_stride", ctypes.c_int64 * 3), ("weight_stride", ctypes.c_int64 * 2),
+                ("state_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
-def make_layout(x_dtype: int, state_width: int, state_stride, weight_stride) -> KdaConvLayout:
+def make_layout(x_dtype: int, state_width: int, state_stride, weight_stride,
+                state_dtype: int = KDA_DTYPE_F32) -> KdaConvLayout:
     return KdaConvLayout(x_dtype, state_width, (ctypes.c_int64 * 3)(*state_stride),
-                         (ctypes.c_int64 * 2)(*weight_stride))
+                         (ctypes.c_int64 * 2)(*weight_stride), state_dtype, 0)
 
 
 def lib_path() -> str:
@@ -237,6 +240,7 @@ def epilogue_range(first: int, count: int, activation: int, out, stream=None) ->
 _SILU_NAMES = ("silu", "swish", True)
 _DTYPES = {torch.bfloat16: KDA_DTYPE_BF16, torch.float16: KDA_DTYPE_F16,
            torch.float32: KDA_DTYPE_F32}
+_STATE_DTYPES = {torch.float32: KDA_DTYPE_F32, torch.bfloat16: KDA_DTYPE_BF16}
 
 
 def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
@@ -245,7 +249,7 @@ def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
     (x CUDA, 2-D, unit channel stride, bf16 / fp16 / fp32; FP32 weight (dim, 4)
     and conv_states (lines, dim, >= 3), any strides; part_dim a multiple of 64
     dividing dim) plus this library's alignment rules (x rows on 16-byte
-    boundaries, state width at most 64)."""
+    boundaries, state width at most 64), widened to a bf16 conv state."""
     if not (x.is_cuda and x.dim() == 2 and x.stride(1) == 1 and x.dtype in _DTYPES):
         return False
     quantum = 4 if x.dtype == torch.float32 else 8
@@ -253,7 +257,7 @@ def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
         x.stride(0) % quantum == 0 and x.data_ptr() % 16 == 0
         and weight.dtype == torch.float32 and weight.dim() == 2
         and weight.size(0) == x.size(1) and weight.size(1) == 4
-        and conv_states.dtype == torch.float32 and conv_states.dim() == 3
+        and conv_states.dtype in _STATE_DTYPES and conv_states.dim() == 3
         and conv_states.size(1) == x.size(1) and 3 <= conv_states.size(2) <= 64
         and part_dim > 0 and part_dim % 64 == 0 and x.size(1) % part_dim == 0
     )
@@ -261,8 +265,10 @@ def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
 
 def layout_of(x: torch.Tensor, weight: torch.Tensor, conv_states: torch.Tensor) -> KdaConvLayout:
     """The kda_conv_layout_t describing these tensors."""
+    if conv_states.dtype not in _STATE_DTYPES:
+        raise TypeError(f"conv_states must be fp32 or bf16, not {conv_states.dtype}")
     return make_layout(_DTYPES[x.dtype], conv_states.size(2), conv_states.stride(),
-                       weight.stride())
+                       weight.stride(), _STATE_DTYPES[conv_states.dtype])
 
 
 def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None,

@@ -97,10 +97,11 @@ struct Params {
     int64_t w_stride_j;
     bool weight_dense;  // strides (4, 1): one float4 per channel
     const float *bias;
-    float *conv_states;
+    void *conv_states;    // fp32, or bf16 when state_bf16
     int state_width;      // K >= 3; the taps read positions K-3 .. K-1
     int64_t s_stride[3];  // element strides of conv_states: line, channel, position
     bool state_dense;     // K == 3 and strides (3 * dim, 3, 1)
+    bool state_bf16;      // stored as bf16: read exactly, written rounded to nearest even
     const int32_t *cache_indices;
     const uint8_t *has_initial_state;
     const int32_t *qsl;
@@ -235,6 +236,71 @@ __device__ __forceinline__ void store_f32_row(float *p, const float (&y)[VEC]) {
         reinterpret_cast<float4 *>(p)[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2],
                                                        y[4 * i + 3]);
     }
+}
+
+// Conv state, dense width 3: the 3 * VEC values of channels c .. c+VEC-1 of a
+// line start at element (line * dim + c) * 3, address sp.  fp32: 12 * VEC bytes, 16-byte
+// aligned (c is a multiple of 4).  bf16: 6 * VEC bytes, 8-byte aligned (dim is
+// a multiple of 64 and c of 4), moved as 8-byte words of four values each.
+__device__ __forceinline__ void *state_line_ptr(const Params &p, int64_t line, int c, bool bf16) {
+    const int64_t off = (line * p.dim + c) * 3;
+    return bf16 ? static_cast<void *>(static_cast<uint16_t *>(p.conv_states) + off)
+                : static_cast<void *>(static_cast<float *>(p.conv_states) + off);
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_state3(const void *sp, bool bf16, float (&st)[3 * VEC]) {
+    if (bf16) {
+#pragma unroll
+        for (int i = 0; i < 3 * VEC / 4; ++i) {
+            const uint2 u = static_cast<const uint2 *>(sp)[i];
+            st[4 * i] = __uint_as_float(u.x << 16);
+            st[4 * i + 1] = __uint_as_float(u.x & 0xFFFF0000u);
+            st[4 * i + 2] = __uint_as_float(u.y << 16);
+            st[4 * i + 3] = __uint_as_float(u.y & 0xFFFF0000u);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 3 * VEC / 4; ++i) {
+            const float4 v4 = static_cast<const float4 *>(sp)[i];
+            st[4 * i] = v4.x;
+            st[4 * i + 1] = v4.y;
+            st[4 * i + 2] = v4.z;
+            st[4 * i + 3] = v4.w;
+        }
+    }
+}
+
+// Stores rows r = 0, 1, 2 of ns as state positions 0, 1, 2 (element 3 v + r).
+template <int VEC>
+__device__ __forceinline__ void store_state3(void *sp, bool bf16, const float (&ns)[3][VEC]) {
+#define KDA_NS(flat) ns[(flat) % 3][(flat) / 3]
+    if (bf16) {
+#pragma unroll
+        for (int i = 0; i < 3 * VEC / 4; ++i)
+            static_cast<uint2 *>(sp)[i] = make_uint2(pack_bf16x2(KDA_NS(4 * i), KDA_NS(4 * i + 1)),
+                               pack_bf16x2(KDA_NS(4 * i + 2), KDA_NS(4 * i + 3)));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 3 * VEC / 4; ++i)
+            static_cast<float4 *>(sp)[i] = make_float4(KDA_NS(4 * i), KDA_NS(4 * i + 1), KDA_NS(4 * i + 2),
+                                KDA_NS(4 * i + 3));
+    }
+#undef KDA_NS
+}
+
+// Conv state element i (any layout), fp32 or bf16.
+__device__ __forceinline__ float state_get(const Params &p, int64_t i) {
+    if (p.state_bf16)
+        return __uint_as_float((uint32_t)static_cast<const uint16_t *>(p.conv_states)[i] << 16);
+    return static_cast<const float *>(p.conv_states)[i];
+}
+
+__device__ __forceinline__ void state_set(const Params &p, int64_t i, float v) {
+    if (p.state_bf16)
+        static_cast<uint16_t *>(p.conv_states)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    else
+        static_cast<float *>(p.conv_states)[i] = v;
 }
 
 // 2^x and 1/x on the special-function unit (PTX ex2.approx.ftz / rcp.approx.ftz:
@@ -390,21 +456,13 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
         const bool read = live && __ldg(p.has_initial_state + s) != 0;
         const int len = e - a;
         if (!kGeneral || p.state_dense) {
-            // Width 3, contiguous: a thread's VEC channels are 12*VEC bytes.
+            // Width 3, contiguous: a thread's VEC channels are 3*VEC values.
+            const bool bf16 = kGeneral && p.state_bf16;
+            void *sp = state_line_ptr(p, line, c, bf16);
             float st[3 * VEC];
 #pragma unroll
             for (int i = 0; i < 3 * VEC; ++i) st[i] = 0.0f;
-            float4 *sp = reinterpret_cast<float4 *>(p.conv_states + (line * p.dim + c) * 3);
-            if (read) {
-#pragma unroll
-                for (int i = 0; i < 3 * VEC / 4; ++i) {
-                    const float4 v4 = sp[i];
-                    st[4 * i] = v4.x;
-                    st[4 * i + 1] = v4.y;
-                    st[4 * i + 2] = v4.z;
-                    st[4 * i + 3] = v4.w;
-                }
-            }
+            if (read) load_state3<VEC>(sp, bf16, st);
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 h0[v] = st[3 * v];
@@ -427,16 +485,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
                         for (int v = 0; v < VEC; ++v) ns[r][v] = (len + r == 1) ? h1[v] : h2[v];
                     }
                 }
-#pragma unroll
-                for (int i = 0; i < 3 * VEC / 4; ++i) {
-                    float o4[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int flat = 4 * i + j;  // = 3 * channel + state index
-                        o4[j] = ns[flat % 3][flat / 3];
-                    }
-                    sp[i] = make_float4(o4[0], o4[1], o4[2], o4[3]);
-                }
+                store_state3<VEC>(sp, bf16, ns);
             }
         } else {
             // Any width K and strides: positions K-3 .. K-1 feed the taps; the
@@ -444,12 +493,12 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
             // Ascending positions read position kk + len before it is written.
             const int K = p.state_width;
             const int64_t s0 = p.s_stride[0], s1 = p.s_stride[1], s2 = p.s_stride[2];
-            float *base = p.conv_states + line * s0 + (int64_t)c * s1;
+            const int64_t base = line * s0 + (int64_t)c * s1;
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
-                h0[v] = read ? base[v * s1 + (K - 3) * s2] : 0.0f;
-                h1[v] = read ? base[v * s1 + (K - 2) * s2] : 0.0f;
-                h2[v] = read ? base[v * s1 + (K - 1) * s2] : 0.0f;
+                h0[v] = read ? state_get(p, base + v * s1 + (K - 3) * s2) : 0.0f;
+                h1[v] = read ? state_get(p, base + v * s1 + (K - 2) * s2) : 0.0f;
+                h2[v] = read ? state_get(p, base + v * s1 + (K - 1) * s2) : 0.0f;
             }
             if (live) {
                 for (int kk = 0; kk < K; ++kk) {
@@ -462,10 +511,10 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
                     } else {
 #pragma unroll
                         for (int v = 0; v < VEC; ++v)
-                            vals[v] = read ? base[v * s1 + (int64_t)(kk + len) * s2] : 0.0f;
+                            vals[v] = read ? state_get(p, base + v * s1 + (kk + len) * s2) : 0.0f;
                     }
 #pragma unroll
-                    for (int v = 0; v < VEC; ++v) base[v * s1 + (int64_t)kk * s2] = vals[v];
+                    for (int v = 0; v < VEC; ++v) state_set(p, base + v * s1 + kk * s2, vals[v]);
                 }
             }
         }
@@ -556,8 +605,12 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 // shifted by one row.  No program search: the grid is tokens x vectors.
 // ---------------------------------------------------------------------------
 
-template <int VEC, int kDtype, bool kGeneral, bool kSilu, bool kBias>
-__global__ void __launch_bounds__(256, kGeneral ? 2 : 4) kda_conv1d_update_kernel(const Params p) {
+// kLayout: 0 dense weight and dense fp32 state; 1 dense weight and dense bf16
+// state; 2 any strides, width and state type (kGeneral).
+template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias>
+__global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
+    kda_conv1d_update_kernel(const Params p) {
+    constexpr bool kGeneral = kLayout == 2;
 #if KDA_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -608,20 +661,12 @@ __global__ void __launch_bounds__(256, kGeneral ? 2 : 4) kda_conv1d_update_kerne
     const bool live = line != p.null_block_id;
     float h0[VEC], h1[VEC], h2[VEC];
     if (!kGeneral || p.state_dense) {
-        float4 *sp = reinterpret_cast<float4 *>(p.conv_states + (line * p.dim + c) * 3);
+        const bool bf16 = kLayout == 1 || (kGeneral && p.state_bf16);
+        void *sp = state_line_ptr(p, line, c, bf16);
         float st[3 * VEC];
 #pragma unroll
         for (int i = 0; i < 3 * VEC; ++i) st[i] = 0.0f;
-        if (live) {
-#pragma unroll
-            for (int i = 0; i < 3 * VEC / 4; ++i) {
-                const float4 v4 = sp[i];
-                st[4 * i] = v4.x;
-                st[4 * i + 1] = v4.y;
-                st[4 * i + 2] = v4.z;
-                st[4 * i + 3] = v4.w;
-            }
-        }
+        if (live) load_state3<VEC>(sp, bf16, st);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
             h0[v] = st[3 * v];
@@ -630,27 +675,24 @@ __global__ void __launch_bounds__(256, kGeneral ? 2 : 4) kda_conv1d_update_kerne
         }
         if (live) {
             // new line: (h1, h2, x) per channel
+            float ns[3][VEC];
 #pragma unroll
-            for (int i = 0; i < 3 * VEC / 4; ++i) {
-                float o4[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int flat = 4 * i + j;
-                    const int v = flat / 3, r = flat % 3;
-                    o4[j] = r == 0 ? h1[v] : (r == 1 ? h2[v] : xv[v]);
-                }
-                sp[i] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            for (int v = 0; v < VEC; ++v) {
+                ns[0][v] = h1[v];
+                ns[1][v] = h2[v];
+                ns[2][v] = xv[v];
             }
+            store_state3<VEC>(sp, bf16, ns);
         }
     } else {
         const int K = p.state_width;
         const int64_t s1 = p.s_stride[1], s2 = p.s_stride[2];
-        float *base = p.conv_states + line * p.s_stride[0] + (int64_t)c * s1;
+        const int64_t base = line * p.s_stride[0] + (int64_t)c * s1;
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
-            h0[v] = live ? base[v * s1 + (K - 3) * s2] : 0.0f;
-            h1[v] = live ? base[v * s1 + (K - 2) * s2] : 0.0f;
-            h2[v] = live ? base[v * s1 + (K - 1) * s2] : 0.0f;
+            h0[v] = live ? state_get(p, base + v * s1 + (K - 3) * s2) : 0.0f;
+            h1[v] = live ? state_get(p, base + v * s1 + (K - 2) * s2) : 0.0f;
+            h2[v] = live ? state_get(p, base + v * s1 + (K - 1) * s2) : 0.0f;
         }
         if (live) {
             // shift by one row (ascending: position kk + 1 is read before it is
@@ -658,8 +700,9 @@ __global__ void __launch_bounds__(256, kGeneral ? 2 : 4) kda_conv1d_update_kerne
 #pragma unroll
             for (int v = 0; v < VEC; ++v) {
                 for (int kk = 0; kk + 1 < K; ++kk)
-                    base[v * s1 + (int64_t)kk * s2] = base[v * s1 + (int64_t)(kk + 1) * s2];
-                base[v * s1 + (int64_t)(K - 1) * s2] = xv[v];
+                    state_set(p, base + v * s1 + (int64_t)kk * s2,
+                              state_get(p, base + v * s1 + (int64_t)(kk + 1) * s2));
+                state_set(p, base + v * s1 + (int64_t)(K - 1) * s2, xv[v]);
             }
         }
     }
@@ -709,6 +752,8 @@ kda_conv_layout_t default_layout(int64_t dim) {
     l.state_stride[2] = 1;
     l.weight_stride[0] = 4;
     l.weight_stride[1] = 1;
+    l.state_dtype = KDA_DTYPE_F32;
+    l.reserved = 0;
     return l;
 }
 
@@ -722,6 +767,7 @@ kda_status_t check_sizes(int64_t x_row_stride, int64_t tokens, int64_t dim, int6
     return KDA_OK;
 }
 
+// Width 3 and strides (3 * dim, 3, 1), whatever the state's storage type.
 bool state_is_dense(const kda_conv_layout_t &l, int64_t dim) {
     return l.state_width == 3 && l.state_stride[0] == 3 * dim && l.state_stride[1] == 3 &&
            l.state_stride[2] == 1;
@@ -733,7 +779,7 @@ bool weight_is_dense(const kda_conv_layout_t &l) {
 
 kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
                         int64_t part_dim, const float *weight, const float *bias,
-                        const float *conv_states, const int32_t *cache_indices,
+                        const void *conv_states, const int32_t *cache_indices,
                         const uint8_t *has_initial_state, const int32_t *query_start_loc,
                         int64_t num_seqs, int activation, const void *out,
                         const kda_conv_layout_t &l, bool need_ranges = true) {
@@ -741,6 +787,8 @@ kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int
     if (st != KDA_OK) return st;
     if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
     if (l.x_dtype != KDA_DTYPE_BF16 && l.x_dtype != KDA_DTYPE_F16 && l.x_dtype != KDA_DTYPE_F32)
+        return KDA_ERR_INVALID_ARG;
+    if ((l.state_dtype != KDA_DTYPE_F32 && l.state_dtype != KDA_DTYPE_BF16) || l.reserved != 0)
         return KDA_ERR_INVALID_ARG;
     if (l.state_width < 3) return KDA_ERR_INVALID_ARG;
     if (l.state_width > kMaxStateWidth) return KDA_ERR_UNSUPPORTED;
@@ -753,8 +801,8 @@ kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int
         (bias && !aligned(bias, 16)))
         return KDA_ERR_MISALIGNED;
     if (weight_is_dense(l) ? !aligned(weight, 16) : !aligned(weight, 4)) return KDA_ERR_MISALIGNED;
-    if (state_is_dense(l, dim) ? !aligned(conv_states, 16) : !aligned(conv_states, 4))
-        return KDA_ERR_MISALIGNED;
+    const uintptr_t state_elem = l.state_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    if (!aligned(conv_states, state_is_dense(l, dim) ? 16 : state_elem)) return KDA_ERR_MISALIGNED;
     return KDA_OK;
 }
 
@@ -865,7 +913,7 @@ void dispatch_act(const Params &p, const Shape &sh, bool silu, cudaStream_t s) {
 
 template <int kDtype>
 void dispatch(const Params &p, const Shape &sh, bool silu, cudaStream_t s) {
-    if (p.weight_dense && p.state_dense)
+    if (p.weight_dense && p.state_dense && !p.state_bf16)
         dispatch_act<kDtype, false>(p, sh, silu, s);
     else
         dispatch_act<kDtype, true>(p, sh, silu, s);
@@ -884,7 +932,7 @@ kda_status_t record_cuda_error() {
 }
 
 kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
-                 int64_t part_dim, const float *weight, const float *bias, float *conv_states,
+                 int64_t part_dim, const float *weight, const float *bias, void *conv_states,
                  const int32_t *cache_indices, const uint8_t *has_initial_state,
                  const int32_t *query_start_loc, int64_t num_seqs, int64_t null_block_id,
                  int activation, void *out, bool preact, const kda_conv_layout_t *layout,
@@ -916,6 +964,7 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.state_width = l.state_width;
     for (int i = 0; i < 3; ++i) p.s_stride[i] = l.state_stride[i];
     p.state_dense = state_is_dense(l, dim);
+    p.state_bf16 = l.state_dtype == KDA_DTYPE_BF16;
     p.cache_indices = cache_indices;
     p.has_initial_state = has_initial_state;
     p.qsl = query_start_loc;
@@ -950,38 +999,43 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     return record_cuda_error();
 }
 
-template <int kDtype, bool kGeneral, bool kSilu, bool kBias>
+template <int kDtype, int kLayout, bool kSilu, bool kBias>
 void launch_update(const Params &p, int64_t blocks, cudaStream_t stream) {
-    launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kGeneral, kSilu, kBias>,
+    launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias>,
                   (unsigned)blocks, 256, p, stream);
 }
 
-template <int kDtype, bool kGeneral>
+template <int kDtype, int kLayout>
 void dispatch_update_act(const Params &p, int64_t blocks, bool silu, cudaStream_t s) {
     if (silu) {
         if (p.bias)
-            launch_update<kDtype, kGeneral, true, true>(p, blocks, s);
+            launch_update<kDtype, kLayout, true, true>(p, blocks, s);
         else
-            launch_update<kDtype, kGeneral, true, false>(p, blocks, s);
+            launch_update<kDtype, kLayout, true, false>(p, blocks, s);
     } else {
         if (p.bias)
-            launch_update<kDtype, kGeneral, false, true>(p, blocks, s);
+            launch_update<kDtype, kLayout, false, true>(p, blocks, s);
         else
-            launch_update<kDtype, kGeneral, false, false>(p, blocks, s);
+            launch_update<kDtype, kLayout, false, false>(p, blocks, s);
     }
 }
 
+// The decode step moves little besides the state lines, so a dense bf16 state
+// has its own lean variant (the general one holds about twice the registers).
 template <int kDtype>
 void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s) {
     if (p.weight_dense && p.state_dense)
-        dispatch_update_act<kDtype, false>(p, blocks, silu, s);
+        if (p.state_bf16)
+            dispatch_update_act<kDtype, 1>(p, blocks, silu, s);
+        else
+            dispatch_update_act<kDtype, 0>(p, blocks, silu, s);
     else
-        dispatch_update_act<kDtype, true>(p, blocks, silu, s);
+        dispatch_update_act<kDtype, 2>(p, blocks, silu, s);
 }
 
 kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
                         int64_t part_dim, const float *weight, const float *bias,
-                        float *conv_states, const int32_t *cache_indices, int64_t null_block_id,
+                        void *conv_states, const int32_t *cache_indices, int64_t null_block_id,
                         int activation, void *out, const kda_conv_layout_t *layout,
                         kda_stream_t stream) {
     const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
@@ -1009,6 +1063,7 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     p.state_width = l.state_width;
     for (int i = 0; i < 3; ++i) p.s_stride[i] = l.state_stride[i];
     p.state_dense = state_is_dense(l, dim);
+    p.state_bf16 = l.state_dtype == KDA_DTYPE_BF16;
     p.cache_indices = cache_indices;
     p.null_block_id = null_block_id;
     p.out = out;
@@ -1041,7 +1096,7 @@ kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t toke
 
 kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t tokens,
                                   int64_t dim, int64_t part_dim, const float *weight,
-                                  const float *bias, float *conv_states,
+                                  const float *bias, void *conv_states,
                                   const int32_t *cache_indices, const uint8_t *has_initial_state,
                                   const int32_t *query_start_loc, int64_t num_seqs,
                                   int64_t null_block_id, int activation, void *out,
@@ -1053,7 +1108,7 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
 
 kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
                               int64_t part_dim, const float *weight, const float *bias,
-                              float *conv_states, const int32_t *cache_indices,
+                              void *conv_states, const int32_t *cache_indices,
                               int64_t null_block_id, int activation, void *out,
                               const kda_conv_layout_t *layout, kda_stream_t stream) {
     return run_update(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
@@ -1086,7 +1141,7 @@ kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, i
 
 kda_status_t kda_packed_conv1d_ex_check_args(
     const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
-    const float *weight, const float *bias, const float *conv_states,
+    const float *weight, const float *bias, const void *conv_states,
     const int32_t *cache_indices, const uint8_t *has_initial_state,
     const int32_t *query_start_loc, int64_t num_seqs, int activation, const void *out,
     const kda_conv_layout_t *layout) {

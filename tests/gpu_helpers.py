@@ -7,9 +7,30 @@ import numpy as np
 import torch
 
 import oracle
+import pins
 import workloads
 
 SENTINEL = -1  # int16 view of the bf16 pattern 0xFFFF (a NaN no conv produces)
+
+
+def state_to_device(states: np.ndarray, dev) -> torch.Tensor:
+    """Host conv states (float32, or uint16 bf16 bits) as a device tensor of
+    the same bytes (float32 or bfloat16), strides kept."""
+    if states.dtype == np.uint16:
+        return torch.from_numpy(states.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(states).to(dev)
+
+
+def state_dtype_of(states: torch.Tensor) -> int:
+    """The kda_dtype_t of a device conv-state tensor."""
+    return 0 if states.dtype == torch.bfloat16 else 2  # KDA_DTYPE_BF16 / KDA_DTYPE_F32
+
+
+def state_to_host(states: torch.Tensor) -> np.ndarray:
+    """The inverse of state_to_device, as a contiguous array."""
+    if states.dtype == torch.bfloat16:
+        return states.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    return states.contiguous().cpu().numpy()
 
 
 def ordered_bf16(bits: np.ndarray) -> np.ndarray:
@@ -39,7 +60,7 @@ class DeviceBatch:
         self.x_buf = torch.from_numpy(b.x_buf.view(np.int16)).to(dev)
         self.weight = torch.from_numpy(b.weight).to(dev)
         self.bias = None if b.bias is None else torch.from_numpy(b.bias).to(dev)
-        self.conv_states = torch.from_numpy(b.conv_states).to(dev)
+        self.conv_states = state_to_device(b.conv_states, dev)
         self.cache_indices = torch.from_numpy(b.cache_indices).to(dev)
         self.has_initial_state = torch.from_numpy(b.has_initial_state).to(dev)
         self.query_start_loc = torch.from_numpy(b.query_start_loc).to(dev)
@@ -60,9 +81,17 @@ class DeviceBatch:
                 b.query_start_loc, self.b.num_seqs, self.b.null_block_id)
 
     def run(self, stream=None) -> None:
+        """kda_packed_conv1d; kda_packed_conv1d_ex with a bf16-state layout
+        when the batch's state is bf16."""
         import linear_attention_prefill_varlen_gb300 as pkg
 
-        pkg.kda_packed_conv1d(*self.args(), self.b.activation, self.out, stream)
+        if self.conv_states.dtype == torch.bfloat16:
+            st = self.conv_states
+            lay = pkg.make_layout(pkg.KDA_DTYPE_BF16, st.size(2), st.stride(), (4, 1),
+                                  pkg.KDA_DTYPE_BF16)
+            pkg.kda_packed_conv1d_ex(*self.args(), self.b.activation, self.out, lay, stream)
+        else:
+            pkg.kda_packed_conv1d(*self.args(), self.b.activation, self.out, stream)
 
     def run_preact(self, stream=None) -> None:
         import linear_attention_prefill_varlen_gb300 as pkg
@@ -73,12 +102,14 @@ class DeviceBatch:
         return self.out.cpu().numpy().view(np.uint16)
 
     def states(self) -> np.ndarray:
-        return self.conv_states.cpu().numpy()
+        return state_to_host(self.conv_states)
 
 
 def oracle_run(b: workloads.Batch, want_preact: bool = False) -> tuple[dict, np.ndarray]:
     """Runs the oracle on a copy of b's state; returns (result, updated states)."""
     st = b.conv_states.copy()
+    if st.dtype == np.uint16:  # bf16 state: the general-layout oracle
+        return pins.run_oracle_ex(b, states=st, want_preact=want_preact), st
     res = oracle.packed_conv1d(b.x_buf, b.col_offset, b.dim, b.part_dim, b.weight, b.bias, st,
                                b.cache_indices, b.has_initial_state, b.query_start_loc,
                                b.null_block_id, b.activation, want_preact=want_preact)
@@ -86,7 +117,8 @@ def oracle_run(b: workloads.Batch, want_preact: bool = False) -> tuple[dict, np.
 
 
 def assert_states_equal(got: np.ndarray, want: np.ndarray) -> None:
-    g, w = got.view(np.uint32), want.view(np.uint32)
+    assert got.dtype == want.dtype and got.shape == want.shape
+    g, w = (got.view(np.uint32), want.view(np.uint32)) if got.dtype == np.float32 else (got, want)
     if not np.array_equal(g, w):
         bad = np.argwhere(g != w)
         raise AssertionError(f"{len(bad)} conv-state words differ; first at {bad[0].tolist()}")

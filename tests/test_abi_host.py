@@ -163,8 +163,11 @@ def test_validate_metadata(kda):
     assert kda.validate_metadata(torch.tensor([0, 2, 5]), torch.tensor([-1, -1]), 8, 4, -1)[0] == 0
 
 
-def _layout(kda, dtype=0, width=3, sstride=(3 * 4608, 3, 1), wstride=(4, 1)):
-    return kda.make_layout(dtype, width, sstride, wstride)
+def _layout(kda, dtype=0, width=3, sstride=(3 * 4608, 3, 1), wstride=(4, 1), sdtype=2,
+            reserved=0):
+    lay = kda.make_layout(dtype, width, sstride, wstride, sdtype)
+    lay.reserved = reserved
+    return lay
 
 
 @pytest.mark.parametrize("lay,over,status", [
@@ -182,6 +185,13 @@ def _layout(kda, dtype=0, width=3, sstride=(3 * 4608, 3, 1), wstride=(4, 1)):
     ({"sstride": (3 * 4608, 1, 4608)}, {"conv_states": A16 + 4}, 0),
     ({}, {"conv_states": A16 + 4}, 3),
     ({"sstride": (3 * 4608, 1, 4608)}, {"conv_states": A16 + 2}, 3),
+    ({"sdtype": 0}, {}, 0),  # bf16 conv state
+    ({"sdtype": 1}, {}, 1),  # fp16 conv state: not offered
+    ({"sdtype": 3}, {}, 1),
+    ({"reserved": 1}, {}, 1),
+    ({"sdtype": 0}, {"conv_states": A16 + 8}, 3),  # dense bf16 state: 16-byte alignment
+    ({"sdtype": 0, "sstride": (3 * 4608, 1, 4608)}, {"conv_states": A16 + 2}, 0),
+    ({"sdtype": 0, "width": 4, "sstride": (4 * 4608, 4, 1)}, {"conv_states": A16 + 2}, 0),
 ])
 def test_layout_checks(kda, lay, over, status):
     a = good_args(**over)
@@ -198,6 +208,27 @@ def test_null_layout_is_the_default(kda):
             a["bias"], a["conv_states"], a["cache_indices"], a["has_initial_state"],
             a["query_start_loc"], a["num_seqs"], a["activation"], a["out"])
     assert kda.check_args_ex(*args, None) == kda.check_args(*args) == 3
+
+
+def test_layout_struct_matches_the_header(kda):
+    """kda_conv_layout_t: two int32, five int64, two int32 (56 bytes, no padding)."""
+    import ctypes
+
+    assert ctypes.sizeof(kda.KdaConvLayout) == 56
+    assert kda.KdaConvLayout.state_dtype.offset == 48
+    lay = kda.make_layout(0, 3, (9, 3, 1), (4, 1))
+    assert lay.state_dtype == kda.KDA_DTYPE_F32 and lay.reserved == 0
+
+
+def test_layout_of_maps_the_state_dtype(kda):
+    x = torch.zeros(8, 128, dtype=torch.float16)
+    w = torch.zeros(128, 4)
+    assert kda.layout_of(x, w, torch.zeros(2, 128, 3)).state_dtype == kda.KDA_DTYPE_F32
+    lay = kda.layout_of(x, w, torch.zeros(2, 128, 5, dtype=torch.bfloat16))
+    assert (lay.state_dtype, lay.x_dtype, lay.state_width) == (kda.KDA_DTYPE_BF16,
+                                                               kda.KDA_DTYPE_F16, 5)
+    with pytest.raises(TypeError):
+        kda.layout_of(x, w, torch.zeros(2, 128, 3, dtype=torch.float16))
 
 
 def test_supported_predicate_rejects_host_tensors(kda):

@@ -16,7 +16,8 @@ import torch
 
 import pins
 import workloads
-from gpu_helpers import ulp_diff
+from gpu_helpers import (assert_states_equal, state_dtype_of, state_to_device, state_to_host,
+                         ulp_diff)
 
 pytestmark = pytest.mark.gpu
 
@@ -46,9 +47,9 @@ def _run_device(b: workloads.Batch, state_mem_order: str = "dense", weight_tap_m
         out = torch.full((b.dim // b.part_dim, b.tokens, b.part_dim), -1, dtype=torch.int16,
                          device=dev)
     if state_mem_order == "dense":
-        st = torch.from_numpy(b.conv_states).to(dev)
+        st = state_to_device(b.conv_states, dev)
     else:
-        st = torch.from_numpy(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1))).to(dev)
+        st = state_to_device(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1)), dev)
         st = st.transpose(1, 2)
     if weight_tap_major:
         w = torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t()
@@ -58,13 +59,14 @@ def _run_device(b: workloads.Batch, state_mem_order: str = "dense", weight_tap_m
     meta = [torch.from_numpy(a).to(dev) for a in
             (b.cache_indices, b.has_initial_state, b.query_start_loc)]
     dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
-    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride())
+    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride(),
+                             state_dtype_of(st))
     esz = 4 if b.x_dtype == "f32" else 2
     pkg.kda_packed_conv1d_ex(x.data_ptr() + esz * b.col_offset, b.row_stride, b.tokens, b.dim,
                              b.part_dim, w, bias, st, meta[0], meta[1], meta[2], b.num_seqs,
                              b.null_block_id, b.activation, out, layout)
     torch.cuda.synchronize()
-    return out.cpu().numpy(), st.contiguous().cpu().numpy()
+    return out.cpu().numpy(), state_to_host(st)
 
 
 def _ordered32(v: np.ndarray) -> np.ndarray:
@@ -101,6 +103,13 @@ CASES = [
     ("f16_k8", 406, [3, 7, 12, 40], 128, 128, 128, 0, {"x_dtype": "f16", "state_width": 8}),
     ("f32_k5_none", 407, [6, 1, 33], 64, 64, 68, 4,
      {"x_dtype": "f32", "state_width": 5, "activation": 0}),
+    ("bf16_state", 408, [1, 2, 3, 70, 150, 5], 256, 128, 264, 8, {"state_dtype": "bf16"}),
+    ("bf16_state_f16_none", 409, [33, 1, 2, 200], 192, 64, 192, 0,
+     {"x_dtype": "f16", "state_dtype": "bf16", "activation": 0}),
+    ("bf16_state_f32", 412, [9, 64, 65, 2], 128, 64, 132, 4,
+     {"x_dtype": "f32", "state_dtype": "bf16"}),
+    ("bf16_state_k6", 413, [1, 4, 7, 40], 128, 128, 128, 0,
+     {"state_dtype": "bf16", "state_width": 6}),
 ]
 
 
@@ -115,7 +124,7 @@ def test_general_layout(case, mem, tap_major):
     st = b.conv_states.copy()
     ref = pins.run_oracle_ex(b, states=st)
     got, got_states = _run_device(b, mem, tap_major)
-    assert np.array_equal(got_states.view(np.uint32), st.view(np.uint32))
+    assert_states_equal(got_states, st)
     _compare(b, got, ref["out"])
 
 
@@ -126,7 +135,7 @@ def test_general_layout_large_f16():
     st = b.conv_states.copy()
     ref = pins.run_oracle_ex(b, states=st)
     got, got_states = _run_device(b)
-    assert np.array_equal(got_states.view(np.uint32), st.view(np.uint32))
+    assert_states_equal(got_states, st)
     _compare(b, got, ref["out"])
 
 
@@ -139,7 +148,7 @@ def test_page_style_wrapper_with_fp16_and_wide_state():
                              x_dtype="f16", state_width=4)
     dev = torch.device("cuda")
     x = torch.from_numpy(b.x_buf.view(np.int16)).to(dev).view(torch.float16)
-    st = torch.from_numpy(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1))).to(dev)
+    st = state_to_device(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1)), dev)
     st = st.transpose(1, 2)
     w = torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t()
     assert pkg.packed_causal_conv1d_supported(x, w, st, b.part_dim)
@@ -152,5 +161,5 @@ def test_page_style_wrapper_with_fp16_and_wide_state():
     ref_st = b.conv_states.copy()
     ref = pins.run_oracle_ex(b, states=ref_st)
     assert out.dtype == torch.float16
-    assert np.array_equal(st.contiguous().cpu().numpy().view(np.uint32), ref_st.view(np.uint32))
+    assert np.array_equal(state_to_host(st).view(np.uint32), ref_st.view(np.uint32))
     _compare(b, out.view(torch.int16).cpu().numpy(), ref["out"])

@@ -64,6 +64,20 @@ def test_workload_outputs_and_states(name):
     assert_outputs_match(d.out_bits(), ref["out"], b.activation)
 
 
+@pytest.mark.parametrize("name", ["tiny", "varlen", "short_decode", "large_nobias"])
+def test_workload_with_bf16_state(name):
+    """The same draws with the conv state rounded to bf16 (through
+    kda_packed_conv1d_ex): states bit-exact, outputs as above."""
+    b = _make(name).copy()
+    b.conv_states = workloads.bf16_bits(torch.from_numpy(b.conv_states))
+    ref, ref_states = oracle_run(b)
+    d = DeviceBatch(b)
+    d.run()
+    torch.cuda.synchronize()
+    assert_states_equal(d.states(), ref_states)
+    assert_outputs_match(d.out_bits(), ref["out"], b.activation)
+
+
 @pytest.mark.parametrize("name", ["tiny", "varlen", "long16k", "large_nobias"])
 def test_workload_preactivation_bit_exact(name):
     b = _make(name)

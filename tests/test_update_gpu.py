@@ -13,7 +13,8 @@ import torch
 
 import pins
 import workloads
-from gpu_helpers import ulp_diff
+from gpu_helpers import (assert_states_equal, state_dtype_of, state_to_device, state_to_host,
+                         ulp_diff)
 from test_general_layout_gpu import _compare
 
 pytestmark = pytest.mark.gpu
@@ -44,21 +45,22 @@ def _run_update(b, position_major=False, tap_major=False):
     out = torch.full((b.dim // b.part_dim, b.tokens, b.part_dim), float("nan") if f32 else -1,
                      dtype=torch.float32 if f32 else torch.int16, device=dev)
     if position_major:
-        st = torch.from_numpy(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1))).to(dev)
+        st = state_to_device(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1)), dev)
         st = st.transpose(1, 2)
     else:
-        st = torch.from_numpy(b.conv_states).to(dev)
+        st = state_to_device(b.conv_states, dev)
     w = (torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t() if tap_major
          else torch.from_numpy(b.weight).to(dev))
     bias = None if b.bias is None else torch.from_numpy(b.bias).to(dev)
     ci = torch.from_numpy(b.cache_indices).to(dev)
     dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
-    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride())
+    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride(),
+                             state_dtype_of(st))
     esz = 4 if f32 else 2
     pkg.kda_conv1d_update(x.data_ptr() + esz * b.col_offset, b.row_stride, b.tokens, b.dim,
                           b.part_dim, w, bias, st, ci, b.null_block_id, b.activation, out, layout)
     torch.cuda.synchronize()
-    return out.cpu().numpy(), st.contiguous().cpu().numpy()
+    return out.cpu().numpy(), state_to_host(st)
 
 
 CASES = [
@@ -68,6 +70,11 @@ CASES = [
     ("f32_none", 504, 64, 128, 128, 132, 4, {"x_dtype": "f32", "activation": 0}),
     ("bf16_k4", 505, 90, 128, 64, 128, 0, {"state_width": 4}),
     ("f16_k6_silu", 506, 33, 256, 256, 256, 0, {"x_dtype": "f16", "state_width": 6}),
+    ("bf16_state_bf16", 507, 300, 256, 128, 264, 8, {"state_dtype": "bf16"}),
+    ("bf16_state_f16_none", 508, 96, 192, 64, 200, 8,
+     {"x_dtype": "f16", "state_dtype": "bf16", "activation": 0}),
+    ("bf16_state_f32", 509, 64, 128, 128, 132, 4, {"x_dtype": "f32", "state_dtype": "bf16"}),
+    ("bf16_state_k5", 510, 50, 128, 64, 128, 0, {"state_dtype": "bf16", "state_width": 5}),
 ]
 
 
@@ -81,14 +88,15 @@ def test_update_matches_oracle(case, position_major, tap_major):
     st = b.conv_states.copy()
     ref = pins.run_oracle_ex(b, states=st)
     got, got_st = _run_update(b, position_major, tap_major)
-    assert np.array_equal(got_st.view(np.uint32), st.view(np.uint32))
+    assert_states_equal(got_st, st)
     _compare(b, got, ref["out"])
 
 
-def test_update_decode_workload_and_repeated_steps():
-    """The 1024-sequence decode batch, three steps in a row: each step's state
-    feeds the next, as in generation."""
-    b = workloads.decode()
+@pytest.mark.parametrize("name", ["decode", "decode_bf16_state"])
+def test_update_decode_workload_and_repeated_steps(name):
+    """The 1024-sequence decode batch (fp32 or bf16 state), three steps in a
+    row: each step's state feeds the next, as in generation."""
+    b = workloads.WORKLOADS[name]()
     b.cache_indices[::97] = b.null_block_id
     dev_states = None
     st = b.conv_states.copy()
@@ -98,7 +106,7 @@ def test_update_decode_workload_and_repeated_steps():
         c.conv_states = st.copy() if dev_states is None else dev_states
         ref = pins.run_oracle_ex(c, states=st)
         got, dev_states = _run_update(c)
-        assert np.array_equal(dev_states.view(np.uint32), st.view(np.uint32)), step
+        assert_states_equal(dev_states, st)
         _compare(c, got, ref["out"])
 
 
@@ -196,3 +204,43 @@ def test_update_in_cuda_graph_replays_with_new_metadata():
         ref = pins.run_oracle_ex(b, states=ref_st)
         assert np.array_equal(st.cpu().numpy().view(np.uint32), ref_st.view(np.uint32))
         _compare(b, out.cpu().numpy(), ref["out"])
+
+
+def test_wrappers_prefill_then_decode_on_a_bf16_state():
+    """packed_causal_conv1d_fn then two causal_conv1d_update steps on one bf16
+    conv-state tensor, as a serving loop runs them, against the oracle."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    dev = torch.device("cuda")
+    dim, part, lines = 384, 128, 12
+    pre = workloads.make_batch("bf16_flow_pre", 701, [40, 3, 1, 77], dim, part, 392, lines,
+                               col_offset=8, his_p=0.5, null_count=1, state_dtype="bf16")
+    st = state_to_device(pre.conv_states, dev)
+    w = torch.from_numpy(pre.weight).to(dev)
+    bias = torch.from_numpy(pre.bias).to(dev)
+    x = torch.from_numpy(pre.x_buf.view(np.int16)).to(dev).view(torch.bfloat16)
+    xs = x[:, pre.col_offset:pre.col_offset + dim]
+    meta = [torch.from_numpy(a).to(dev) for a in
+            (pre.query_start_loc, pre.cache_indices, pre.has_initial_state)]
+    assert pkg.packed_causal_conv1d_supported(xs, w, st, part)
+    out = pkg.packed_causal_conv1d_fn(xs, w, bias, st, meta[0], meta[1], meta[2].bool(), part,
+                                      activation="silu", null_block_id=pre.null_block_id)
+    ref_st = pre.conv_states.copy()
+    ref = pins.run_oracle_ex(pre, states=ref_st)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16
+    assert_states_equal(state_to_host(st), ref_st)
+    _compare(pre, out.view(torch.int16).cpu().numpy(), ref["out"])
+    for step in range(2):
+        d = workloads.make_batch(f"bf16_flow_dec{step}", 710 + step, [1] * 4, dim, part, 392,
+                                 lines, col_offset=8, state_dtype="bf16")
+        d.weight, d.bias, d.cache_indices = pre.weight, pre.bias, pre.cache_indices.copy()
+        d.has_initial_state[:] = 1
+        xd = torch.from_numpy(d.x_buf.view(np.int16)).to(dev).view(torch.bfloat16)
+        ci = torch.from_numpy(d.cache_indices).to(dev)
+        o = pkg.causal_conv1d_update(xd[:, d.col_offset:d.col_offset + dim], st, w, bias, ci,
+                                     part, activation="silu", null_block_id=d.null_block_id)
+        ref = pins.run_oracle_ex(d, states=ref_st)
+        torch.cuda.synchronize()
+        assert_states_equal(state_to_host(st), ref_st)
+        _compare(d, o.view(torch.int16).cpu().numpy(), ref["out"])

@@ -24,6 +24,7 @@ token prefill chunks, row-strided bf16 slices of a wider projection):
                 weight U(-1, 1), no bias, no activation, seed 4
   decode        1024 sequences of 1 token (a decode step), dim 4608, row stride
                 6400, 2048 cache lines, every sequence with an initial state, seed 5
+  decode_bf16_state  the decode draws with the conv state rounded to bf16
 """
 
 from __future__ import annotations
@@ -47,7 +48,7 @@ class Batch:
     part_dim: int
     weight: np.ndarray  # (dim, 4) float32
     bias: np.ndarray | None  # (dim,) float32
-    conv_states: np.ndarray  # (cache_lines, dim, 3) float32
+    conv_states: np.ndarray  # (cache_lines, dim, K) float32, or uint16 bf16 bits
     cache_indices: np.ndarray  # (num_seqs,) int32
     has_initial_state: np.ndarray  # (num_seqs,) uint8 (0/1)
     query_start_loc: np.ndarray  # (num_seqs + 1,) int32
@@ -83,14 +84,14 @@ class Batch:
             dict(self.notes), self.x_dtype)
 
 
-def _bf16_bits(t: torch.Tensor) -> np.ndarray:
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.to(torch.bfloat16).contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
 def _x_storage(t: torch.Tensor, x_dtype: str) -> np.ndarray:
     """fp32 samples stored as the call's x type, by torch's own conversion."""
     if x_dtype == "bf16":
-        return _bf16_bits(t)
+        return bf16_bits(t)
     if x_dtype == "f16":
         return t.to(torch.float16).contiguous().view(torch.int16).numpy().view(np.uint16)
     assert x_dtype == "f32"
@@ -102,12 +103,13 @@ def make_batch(name: str, seed: int, lengths, dim: int, part_dim: int, row_strid
                w_range: float = 0.5, bias_std: float | None = 0.1, activation: int = 1,
                his_p: float = 1.0, his: list[int] | None = None, null_count: int = 0,
                tokens: int | None = None, first_token: int = 0, x_dtype: str = "bf16",
-               state_width: int = 3) -> Batch:
+               state_width: int = 3, state_dtype: str = "f32") -> Batch:
     """Draws one batch.
 
     Draw order: lengths are given; x (tokens, row_stride) ~ N(0, x_std^2);
     weight (dim, 4) ~ U(-w_range, w_range); bias (dim) ~ N(0, bias_std^2) if
-    bias_std is not None; conv_states (cache_lines, dim, 3) ~ N(0, 1);
+    bias_std is not None; conv_states (cache_lines, dim, state_width) ~ N(0, 1),
+    kept as float32 or (state_dtype "bf16") rounded to bf16 bits by torch;
     cache_indices = the first num_seqs of a random permutation of the cache
     lines; has_initial_state ~ Bernoulli(his_p) unless given; then
     `null_count` distinct random sequences get NULL_BLOCK_ID as cache index.
@@ -129,7 +131,12 @@ def make_batch(name: str, seed: int, lengths, dim: int, part_dim: int, row_strid
     b = None
     if bias_std is not None:
         b = (torch.randn(dim, generator=g) * bias_std).numpy().astype(np.float32)
-    s = torch.randn(cache_lines, dim, state_width, generator=g).numpy().astype(np.float32)
+    s_draw = torch.randn(cache_lines, dim, state_width, generator=g)
+    if state_dtype == "bf16":
+        s = bf16_bits(s_draw)
+    else:
+        assert state_dtype == "f32"
+        s = s_draw.numpy().astype(np.float32)
     assert n <= cache_lines
     ci = torch.randperm(cache_lines, generator=g)[:n].numpy().astype(np.int32)
     if his is None:
@@ -180,6 +187,12 @@ def decode() -> Batch:
     return make_batch("decode", 5, [1] * 1024, 4608, 1536, 6400, 2048, his_p=1.0)
 
 
+def decode_bf16_state() -> Batch:
+    """The decode step with the conv state stored as bf16."""
+    return make_batch("decode_bf16_state", 5, [1] * 1024, 4608, 1536, 6400, 2048, his_p=1.0,
+                      state_dtype="bf16")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "varlen": varlen,
@@ -187,6 +200,7 @@ WORKLOADS = {
     "short_decode": short_decode,
     "large_nobias": large_nobias,
     "decode": decode,
+    "decode_bf16_state": decode_bf16_state,
 }
 
 
@@ -203,6 +217,6 @@ def algorithmic_bytes(b: Batch) -> int:
     writes = int(np.count_nonzero(live & not_null))
     d = b.dim
     xb = 4 if b.x_dtype == "f32" else 2
-    sb = 4 * b.conv_states.shape[2]
+    sb = b.conv_states.itemsize * b.conv_states.shape[2]
     return (2 * xb * rows * d + sb * d * reads + sb * d * writes + 16 * d
             + (4 * d if b.bias is not None else 0))
