@@ -1,7 +1,7 @@
 """CPU oracle for the packed varlen causal depthwise conv1d (test infrastructure).
 
-Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The product path (the CUDA library and
+Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg and reference (oracle) arm may import this package.  The product path (the CUDA library and
 its Python binding) never touches it, and it never touches the product path.
 
 The arithmetic lives in ``kda_conv_ref.c`` (plain single-threaded C, FP32 as
