@@ -366,7 +366,13 @@ __host__ __device__ constexpr int min_blocks() {
 
 // kGeneral: the weight and the conv state may have any strides and the state
 // any width K; otherwise both are dense (weight (dim, 4), state (lines, dim, 3)).
-template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
+// kShort: programs with fewer rows than the queue take a path that computes
+// only their rows.  It is a separate instantiation, chosen by the host for
+// batches of short sequences: its mere presence costs the long-chunk path
+// about 3 % on GB300 (register allocation and scheduling of the main loop
+// shift), while it saves 10-15 % on batches of one- to five-token sequences.
+template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias,
+          bool kShort>
 __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
     kda_packed_conv1d_kernel(const Params p) {
 #if KDA_PDL
@@ -569,6 +575,39 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
         xnext += P * xs;
         o += P * out_row;
     };
+    if constexpr (kShort) {
+        if (t1 - t0 < P) {
+            // Every row of the chunk is in the queue already: compute those
+            // rows only (the checked step below computes all P).
+            const int n = t1 - t0;
+#pragma unroll
+            for (int u = 0; u < P; ++u) {
+                if (u >= n) break;
+                float xv[VEC];
+                widen<VEC, kDtype>(q[u], xv);
+                float y[VEC];
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    float acc = kBias ? bias[v] : 0.0f;
+                    acc = __fmaf_rn(h0[v], w[v][0], acc);
+                    acc = __fmaf_rn(h1[v], w[v][1], acc);
+                    acc = __fmaf_rn(h2[v], w[v][2], acc);
+                    acc = __fmaf_rn(xv[v], w[v][3], acc);
+                    y[v] = acc;
+                    h0[v] = h1[v];
+                    h1[v] = h2[v];
+                    h2[v] = xv[v];
+                }
+                if constexpr (kSilu) silu_row<VEC>(y);
+                OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
+                if constexpr (kPreact)
+                    store_f32_row<VEC>(dst, y);
+                else
+                    store_out_row<VEC, kDtype>(dst, y);
+            }
+            return;
+        }
+    }
     for (; t + 2 * P <= t1; t += P) rows(std::false_type{});
     for (; t < t1; t += P) rows(std::true_type{});
 }
@@ -813,6 +852,7 @@ struct Shape {
     int64_t programs;
     int warps_per_prog;
     int64_t total_warps;
+    bool short_seqs;  // mean sequence length below the queue depth: the kShort kernel
 };
 
 // Chunk length.  The resident-warp budget is waves x SMs x warps per SM.
@@ -842,6 +882,7 @@ Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
     sh.chunk = (int)chunk;
     sh.programs = (tokens + sh.chunk - 1) / sh.chunk + num_seqs;
     sh.total_warps = sh.programs * sh.warps_per_prog;
+    sh.short_seqs = tokens < (int64_t)kQueue * num_seqs;
     const int64_t warps_per_cta = kThreads / 32;
     sh.ctas = (sh.total_warps + warps_per_cta - 1) / warps_per_cta;
     return sh;
@@ -892,8 +933,14 @@ void launch_kernel(void (*kernel)(Params), unsigned blocks, unsigned threads, co
 
 template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
 void launch(const Params &p, const Shape &sh, cudaStream_t stream) {
-    launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias>,
-                  (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+    if (sh.short_seqs)
+        launch_kernel(
+            kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias, true>,
+            (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+    else
+        launch_kernel(
+            kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias, false>,
+            (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
 }
 
 template <int kDtype, bool kGeneral>

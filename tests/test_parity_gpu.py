@@ -78,7 +78,7 @@ def test_workload_with_bf16_state(name):
     assert_outputs_match(d.out_bits(), ref["out"], b.activation)
 
 
-@pytest.mark.parametrize("name", ["tiny", "varlen", "long16k", "large_nobias"])
+@pytest.mark.parametrize("name", ["tiny", "varlen", "long16k", "large_nobias", "spec_decode"])
 def test_workload_preactivation_bit_exact(name):
     b = _make(name)
     ref, ref_states = oracle_run(b, want_preact=True)
@@ -103,6 +103,10 @@ SWEEP = [
     (206, [17, 250, 33, 64, 128, 3], 384, 192, 400, 16, {"his_p": 0.3, "null_count": 2}),
     (207, [1000, 1, 999], 64, 64, 72, 8, {"activation": 0}),
     (208, [2, 2, 2, 2], 1088, 1088, 1096, 8, {"bias": False}),
+    # mean length below the queue depth: the short-sequence instantiation, with
+    # programs both shorter and longer than the queue
+    (209, [1, 2, 3, 4, 5, 6, 7, 8, 9, 13, 1, 1, 1, 1, 1, 1], 256, 128, 264, 8, {"his_p": 0.5}),
+    (210, [0, 5, 0, 1, 2, 0, 4], 192, 64, 200, 8, {"activation": 0}),
 ]
 
 

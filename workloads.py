@@ -25,6 +25,9 @@ token prefill chunks, row-strided bf16 slices of a wider projection):
   decode        1024 sequences of 1 token (a decode step), dim 4608, row stride
                 6400, 2048 cache lines, every sequence with an initial state, seed 5
   decode_bf16_state  the decode draws with the conv state rounded to bf16
+  spec_decode   1024 sequences of 4 tokens (a speculative-decoding verification
+                step: one accepted token plus three drafts), dim 4608, row stride
+                6400, 2048 cache lines, every sequence with an initial state, seed 6
 """
 
 from __future__ import annotations
@@ -193,6 +196,11 @@ def decode_bf16_state() -> Batch:
                       state_dtype="bf16")
 
 
+def spec_decode() -> Batch:
+    """1024 sequences of 4 tokens each, 2048 cache lines."""
+    return make_batch("spec_decode", 6, [4] * 1024, 4608, 1536, 6400, 2048, his_p=1.0)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "varlen": varlen,
@@ -201,6 +209,7 @@ WORKLOADS = {
     "large_nobias": large_nobias,
     "decode": decode,
     "decode_bf16_state": decode_bf16_state,
+    "spec_decode": spec_decode,
 }
 
 
