@@ -3,9 +3,9 @@
 // The operation is the one the vLLM page "vllm.models.kimi_k3.nvidia.ops.kda_conv"
 // describes (module docstring and packed_causal_conv1d_fn): a row-strided x
 // (tokens, dim) is read in place, each channel is convolved causally over its
-// sequence with 4 FP32 taps (history rows from an FP32 paged conv state), SiLU is
-// optional, and the result is rounded to x's type (nearest even) into dense
-// (tokens, part_dim) planes.  The exact per-element arithmetic is spelled out in
+// sequence with 4 FP32 taps (history rows from a paged conv state, FP32 as on
+// the page or optionally bf16), SiLU is optional, and the result is rounded to
+// x's type (nearest even) into dense (tokens, part_dim) planes.  The exact per-element arithmetic is spelled out in
 // include/kda_conv.h.
 //
 // Design (memory-bound stencil, no contraction, so no tensor cores):

@@ -37,18 +37,20 @@ def _margins_intact(buf: torch.Tensor, nbytes: int) -> bool:
     return bool(head.eq(0xA5).all().item() and tail.eq(0xA5).all().item())
 
 
-@pytest.mark.parametrize("entry,x_dtype,width", [
-    ("packed", "bf16", 3), ("ex", "f16", 3), ("ex", "f32", 5), ("update", "bf16", 3),
-    ("update", "f32", 4),
+@pytest.mark.parametrize("entry,x_dtype,width,state_dtype", [
+    ("packed", "bf16", 3, "f32"), ("ex", "f16", 3, "f32"), ("ex", "f32", 5, "f32"),
+    ("update", "bf16", 3, "f32"), ("update", "f32", 4, "f32"),
+    ("ex", "bf16", 3, "bf16"), ("ex", "f16", 6, "bf16"), ("update", "bf16", 3, "bf16"),
+    ("update", "f32", 5, "bf16"),
 ])
-def test_writes_stay_inside_out_and_states(entry, x_dtype, width):
+def test_writes_stay_inside_out_and_states(entry, x_dtype, width, state_dtype):
     import linear_attention_prefill_varlen_gb300 as pkg
 
     dev = torch.device("cuda")
     lengths = [1] * 40 if entry == "update" else [1, 2, 3, 70, 200, 5]
     b = workloads.make_batch(f"guard_{entry}", 901, lengths, 256, 128, 264, len(lengths) + 2,
                              col_offset=8, his_p=0.6, null_count=2, x_dtype=x_dtype,
-                             state_width=width)
+                             state_width=width, state_dtype=state_dtype)
     if entry == "update":
         b.has_initial_state[:] = 1
     esz = 4 if x_dtype == "f32" else 2
@@ -63,7 +65,8 @@ def test_writes_stay_inside_out_and_states(entry, x_dtype, width):
     ci, his, qsl = (torch.from_numpy(a).to(dev) for a in
                     (b.cache_indices, b.has_initial_state, b.query_start_loc))
     dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
-    layout = pkg.make_layout(dt[x_dtype], width, (width * b.dim, width, 1), (4, 1))
+    layout = pkg.make_layout(dt[x_dtype], width, (width * b.dim, width, 1), (4, 1),
+                             dt[state_dtype])
     xp = x.data_ptr() + esz * b.col_offset
     if entry == "packed":
         pkg.kda_packed_conv1d(xp, b.row_stride, b.tokens, b.dim, b.part_dim, w, bias, sptr, ci,
@@ -79,9 +82,9 @@ def test_writes_stay_inside_out_and_states(entry, x_dtype, width):
     assert _margins_intact(obuf, out_bytes), "write outside the output planes"
     assert _margins_intact(sbuf, st_bytes), "write outside the conv-state array"
     # the null-block lines and unreferenced lines are untouched inside the array
-    got = sbuf[MARGIN:MARGIN + st_bytes].cpu().numpy().view(np.float32).reshape(
+    got = sbuf[MARGIN:MARGIN + st_bytes].cpu().numpy().view(b.conv_states.dtype).reshape(
         b.conv_states.shape)
     live = {int(c) for c in b.cache_indices if c != b.null_block_id}
     for line in range(b.conv_states.shape[0]):
         if line not in live:
-            assert np.array_equal(got[line].view(np.uint32), b.conv_states[line].view(np.uint32))
+            assert got[line].tobytes() == b.conv_states[line].tobytes()
