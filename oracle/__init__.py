@@ -80,6 +80,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_int, P, P,  # activation, out, preact
     ]
     lib.kda_ref_packed_conv1d_ex.restype = ctypes.c_int
+    lib.kda_ref_l2norm_heads.argtypes = [P, I64, I64, I64, ctypes.c_double, P]
+    lib.kda_ref_l2norm_heads.restype = ctypes.c_int
     return lib
 
 
@@ -273,3 +275,52 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
     if want_preact:
         res["preact"] = preact
     return res
+
+
+def l2norm_heads(y: np.ndarray, head_dim: int, eps: float,
+                 lib: ctypes.CDLL | None = None) -> np.ndarray:
+    """The per-head L2 norm of (rows, width) fp32 values, in float64."""
+    lib = lib or load()
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    assert y.ndim == 2
+    out = np.empty(y.shape, dtype=np.float64)
+    rc = lib.kda_ref_l2norm_heads(y.ctypes.data, y.shape[0], y.shape[1], head_dim, float(eps),
+                                  out.ctypes.data)
+    if rc != REF_OK:
+        raise ValueError(f"oracle rejected the call: status {rc}")
+    return out
+
+
+def packed_conv1d_l2norm(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int,
+                         part_dim: int, weight: np.ndarray, bias: np.ndarray | None,
+                         conv_states: np.ndarray, cache_indices, has_initial_state,
+                         query_start_loc, null_block_id: int, activation: int,
+                         norm_planes: int, head_dim: int, eps: float,
+                         lib: ctypes.CDLL | None = None) -> dict:
+    """The conv with the q/k L2 norm folded in: the planes whose bit is set in
+    ``norm_planes`` hold each token's heads divided by their L2 norm.
+
+    Steps, each an oracle function: the general-layout conv (its FP32
+    pre-activations; the conv state is updated as by packed_conv1d_ex), the
+    FP32 activation, the per-head norm in float64, rounding to float32 and then
+    to x's storage type.  Planes outside the mask are the plain conv output.
+    Returns ``out`` as packed_conv1d_ex does."""
+    lib = lib or load()
+    res = packed_conv1d_ex(x_buf, dtype, col_offset, dim, part_dim, weight, bias, conv_states,
+                           cache_indices, has_initial_state, query_start_loc, null_block_id,
+                           activation, want_preact=True, lib=lib)
+    pre = res["preact"]
+    out = res["out"]
+    post = silu(pre, lib) if activation else pre
+    for plane in range(dim // part_dim):
+        if not (norm_planes >> plane) & 1:
+            continue
+        rows = ~np.isnan(pre[plane][:, 0])  # token rows some sequence wrote
+        normed = l2norm_heads(post[plane][rows], head_dim, eps, lib).astype(np.float32)
+        if dtype == DTYPE_BF16:
+            out[plane][rows] = bf16_rne(normed, lib)
+        elif dtype == DTYPE_F16:
+            out[plane][rows] = f16_rne(normed, lib)
+        else:
+            out[plane][rows] = normed
+    return {"out": out}

@@ -384,3 +384,32 @@ int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int
     }
     return REF_OK;
 }
+
+/*
+ * The q/k L2 norm, per token and head.  "vllm.models.kimi_k3.amd.ops.
+ * kda_prefill" (chunk_kda_prefill: q and k are [1, T, H, K]; its
+ * use_qk_l2norm_in_kernel parameter folds "the q/k L2 norm" into the kernel,
+ * and the fused path's comment says its prologue takes over that norm) norms
+ * each head's K channels of a token.  The pages print neither the formula's
+ * epsilon nor its precision.  The reading: out = y / sqrt(sum over the head
+ * of y^2 + eps), eps a caller argument, computed here in double from the FP32
+ * conv outputs y (after the activation).
+ *
+ * y is rows x width floats (width = heads * head_dim, head h at columns
+ * h*head_dim .. (h+1)*head_dim - 1); out receives rows x width doubles.
+ */
+int kda_ref_l2norm_heads(const float *y, int64_t rows, int64_t width, int64_t head_dim,
+                         double eps, double *out) {
+    if (rows < 0 || width < 0 || head_dim <= 0 || width % head_dim != 0) return REF_BAD_SHAPE;
+    if (!(eps >= 0.0)) return REF_BAD_SHAPE;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t h0 = 0; h0 < width; h0 += head_dim) {
+            const float *v = y + r * width + h0;
+            double ss = 0.0;
+            for (int64_t i = 0; i < head_dim; ++i) ss += (double)v[i] * (double)v[i];
+            double d = sqrt(ss + eps);
+            for (int64_t i = 0; i < head_dim; ++i) out[r * width + h0 + i] = (double)v[i] / d;
+        }
+    }
+    return REF_OK;
+}

@@ -723,3 +723,78 @@ def pin_ex_bf16_state(lib) -> None:
 
 
 ALL_PINS.append(pin_ex_bf16_state)
+
+
+# --- the q/k L2 norm ("vllm.models.kimi_k3.amd.ops.kda_prefill": chunk_kda_prefill,
+# use_qk_l2norm_in_kernel; q and k are [1, T, H, K], normed per token and head) ---
+
+def pin_l2norm_closed_forms(lib) -> None:
+    """Hand-worked heads: a 3-4-5 triangle, a lone entry with eps inside the
+    root (1 / sqrt(1 + 3) = 1/2), a negative entry, an all-zero head."""
+    y = np.array([[3, 4, 0, 0, 1, 0, 0, 0, -2, 0, 0, 0, 0, 0, 0, 0]], np.float32)
+    got = oracle.l2norm_heads(y, 4, 0.0, lib)
+    assert got[0, :4].tolist() == [3 / 5, 4 / 5, 0.0, 0.0]
+    assert got[0, 4:8].tolist() == [1.0, 0.0, 0.0, 0.0]
+    assert got[0, 8:12].tolist() == [-1.0, 0.0, 0.0, 0.0]
+    got = oracle.l2norm_heads(y, 4, 3.0, lib)
+    assert got[0, 4] == 0.5 and got[0, 8] == -2 / np.sqrt(7.0)
+    assert got[0, 12:].tolist() == [0.0] * 4  # zero head, eps > 0: zeros
+
+
+def pin_l2norm_invariants(lib) -> None:
+    """On random heads: the squared norm of a result is ss / (ss + eps); every
+    entry of a head is scaled by one positive factor; heads do not interact;
+    scaling the input by 4 leaves an eps = 0 result bit-identical."""
+    g = torch.Generator().manual_seed(71)
+    y = (torch.randn(7, 192, generator=g) * torch.rand(7, 1, generator=g) * 3).numpy()
+    y = y.astype(np.float32)
+    eps = 1e-6
+    got = oracle.l2norm_heads(y, 64, eps, lib)
+    for h in range(3):
+        yh = y[:, 64 * h:64 * (h + 1)].astype(np.float64)
+        gh = got[:, 64 * h:64 * (h + 1)]
+        ss = (yh * yh).sum(axis=1)
+        assert np.allclose((gh * gh).sum(axis=1), ss / (ss + eps), rtol=1e-12, atol=0)
+        ratio = gh / yh
+        assert (ratio > 0).all()
+        assert np.allclose(ratio, ratio[:, :1], rtol=1e-14, atol=0)
+    y2 = y.copy()
+    y2[:, 64:128] *= -7.5
+    got2 = oracle.l2norm_heads(y2, 64, eps, lib)
+    assert np.array_equal(got2[:, :64], got[:, :64]) and np.array_equal(got2[:, 128:], got[:, 128:])
+    a = oracle.l2norm_heads(y, 64, 0.0, lib)
+    assert np.array_equal(oracle.l2norm_heads(y * 4, 64, 0.0, lib), a)
+
+
+def run_oracle_l2norm(b: workloads.Batch, norm_planes: int, head_dim: int, eps: float,
+                      lib=None, states=None) -> dict:
+    return oracle.packed_conv1d_l2norm(
+        b.x_buf, DT[b.x_dtype], b.col_offset, b.dim, b.part_dim, b.weight, b.bias,
+        b.conv_states if states is None else states, b.cache_indices, b.has_initial_state,
+        b.query_start_loc, b.null_block_id, b.activation, norm_planes, head_dim, eps, lib=lib)
+
+
+def pin_l2norm_conv(lib) -> None:
+    """The conv with the norm folded in: planes outside the mask and the conv
+    state are exactly the plain conv's; a normed plane's written rows have
+    heads of unit length up to bf16 rounding; unwritten rows stay untouched;
+    an empty mask is the plain conv."""
+    b = workloads.make_batch("l2conv", 181, [1, 2, 7, 40], 192, 64, 200, 7, col_offset=8,
+                             his_p=0.6, null_count=1, tokens=55)
+    st_plain, st_norm = b.conv_states.copy(), b.conv_states.copy()
+    plain = run_oracle_ex(b, lib, states=st_plain)["out"]
+    normed = run_oracle_l2norm(b, 0b011, 32, 1e-6, lib, states=st_norm)["out"]
+    assert np.array_equal(st_plain.view(np.uint32), st_norm.view(np.uint32))
+    assert np.array_equal(normed[2], plain[2])
+    written = plain[0][:, 0] != 0xFFFF
+    assert (~written).sum() == 55 - 50
+    for plane in (0, 1):
+        assert (normed[plane][~written] == 0xFFFF).all()
+        v = torch_bf16_to_f32(normed[plane][written]).astype(np.float64).reshape(-1, 2, 32)
+        sq = (v * v).sum(axis=2)
+        assert np.all(np.abs(sq - 1.0) < 2.0 ** -6), float(np.abs(sq - 1).max())
+    st3 = b.conv_states.copy()
+    assert np.array_equal(run_oracle_l2norm(b, 0, 32, 1e-6, lib, states=st3)["out"], plain)
+
+
+ALL_PINS += [pin_l2norm_closed_forms, pin_l2norm_invariants, pin_l2norm_conv]

@@ -51,6 +51,12 @@ MUTANTS = [
     # stays in bounds: bf16 stores into an fp32 state only touch the array's own bytes
     ("state_stored_as_bf16_always", "ref_store(conv_states, state_dtype,",
      "ref_store(conv_states, REF_DTYPE_BF16,"),
+    # the q/k L2 norm
+    ("l2_eps_outside_root", "double d = sqrt(ss + eps);", "double d = sqrt(ss) + eps;"),
+    ("l2_no_root", "double d = sqrt(ss + eps);", "double d = ss + eps;"),
+    ("l2_abs_not_square", "ss += (double)v[i] * (double)v[i];", "ss += fabs((double)v[i]);"),
+    ("l2_last_channel_dropped", "for (int64_t i = 0; i < head_dim; ++i) ss +=",
+     "for (int64_t i = 0; i + 1 < head_dim; ++i) ss +="),
 ]
 
 
