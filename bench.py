@@ -65,6 +65,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--qk-l2norm", action="store_true",
+                    help="the *_l2norm entry points: planes 0 and 1 normalised per 128-channel "
+                         "head (eps 1e-6); the cpu_baseline stays the plain conv oracle")
     return ap.parse_args(argv)
 
 
@@ -90,6 +93,8 @@ def kernel_sha() -> str:
 
 def profile_path(entry: str, workload: str) -> str:
     kernel = "kda_conv1d_update" if entry == "update" else "kda_packed_conv1d"
+    if NORM is not None:
+        kernel += "_l2norm"
     return os.path.join(PROFILES, f"{kernel}_{workload}.md")
 
 
@@ -242,9 +247,26 @@ def state_layout(pkg, states: torch.Tensor):
                            pkg.KDA_DTYPE_BF16)
 
 
+NORM = None  # --qk-l2norm: planes 0 and 1 normalised per 128-channel head
+
+
 def call(pkg, b: workloads.Batch, s: dict, stream) -> None:
     if "layout" not in s:
         s["layout"] = state_layout(pkg, s["conv_states"])
+    if NORM is not None:
+        lay = s["layout"] or pkg.make_layout(pkg.KDA_DTYPE_BF16, 3, (3 * b.dim, 3, 1), (4, 1))
+        if ENTRY == "update":
+            pkg.kda_conv1d_update_l2norm(
+                s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim, s["weight"],
+                s["bias"], s["conv_states"], s["cache_indices"], b.null_block_id, b.activation,
+                s["out"], lay, NORM, stream)
+        else:
+            pkg.kda_packed_conv1d_l2norm(
+                s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim, s["weight"],
+                s["bias"], s["conv_states"], s["cache_indices"], s["has_initial_state"],
+                s["query_start_loc"], b.num_seqs, b.null_block_id, b.activation, s["out"], lay,
+                NORM, stream)
+        return
     if ENTRY == "update":
         pkg.kda_conv1d_update(s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim,
                               s["weight"], s["bias"], s["conv_states"], s["cache_indices"],
@@ -568,15 +590,22 @@ def run_ours(args) -> None:
                                 "the per-launch events); value from the launches' own time")
     line["config"]["kernel_source_sha"] = kernel_sha()
     line["config"]["entry"] = "kda_conv1d_update" if ENTRY == "update" else "kda_packed_conv1d"
+    if NORM is not None:
+        line["config"]["entry"] += "_l2norm"
+        line["config"]["qk_l2norm"] = {"planes": [0, 1], "head_dim": 128, "eps": 1e-6}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(b, args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
 def main(argv=None) -> None:
-    global ENTRY
+    global ENTRY, NORM
     args = parse_args(argv)
     ENTRY = args.entry
+    if args.qk_l2norm and args.impl == "ours":
+        import linear_attention_prefill_varlen_gb300 as pkg
+
+        NORM = pkg.make_l2norm(0b011, 128, 1e-6)
     if args.impl == "reference":
         run_reference(args)
     else:

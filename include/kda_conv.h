@@ -185,6 +185,66 @@ kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batc
                               const kda_conv_layout_t *layout, kda_stream_t stream);
 
 /*
+ * The q/k L2 norm folded into the conv's epilogue, after the vLLM page
+ * "vllm.models.kimi_k3.amd.ops.kda_prefill": chunk_kda_prefill takes q and k
+ * as [1, T, H, K], and its use_qk_l2norm_in_kernel parameter and the fused
+ * path's comment have the kernel that consumes them norm each token's heads
+ * itself. Done here instead, the Q and K planes leave the conv normalised.
+ * The norm costs no extra pass over memory.
+ * The pages print neither the epsilon nor the precision. This library's
+ * reading: for each token and each head of head_dim consecutive channels of a
+ * selected plane, with y the FP32 conv output after the activation,
+ *     y = y / sqrt(sum over the head of y^2 + eps)
+ * computed in FP32 (the sum over lanes in a butterfly, the reciprocal root on
+ * the special-function unit, relative error about 2^-23) before the rounding
+ * to x's type.
+ *   plane_mask  bit i: normalise output plane i (Q|K|V packing: 0x3 for q, k).
+ *               0 = no norm. Bits at or above dim / part_dim are an error.
+ *   head_dim    channels per head: 4, 8, 16, 32, 64 or 128, dividing part_dim.
+ *   eps         >= 0, finite. With eps = 0 an all-zero head gives NaN.
+ *   reserved    must be 0.
+ */
+typedef struct kda_l2norm {
+    uint32_t plane_mask;
+    int32_t head_dim;
+    float eps;
+    int32_t reserved;
+} kda_l2norm_t;
+
+/*
+ * kda_packed_conv1d_l2norm -- kda_packed_conv1d_ex, then the L2 norm above on
+ * the planes norm->plane_mask selects. norm NULL or plane_mask 0 is
+ * kda_packed_conv1d_ex itself. The conv state is updated exactly as without
+ * the norm. Invalid norm options return KDA_ERR_INVALID_ARG (mask, eps,
+ * reserved) or KDA_ERR_UNSUPPORTED (head_dim) before any launch.
+ */
+kda_status_t kda_packed_conv1d_l2norm(const void *x, int64_t x_row_stride, int64_t tokens,
+                                      int64_t dim, int64_t part_dim, const float *weight,
+                                      const float *bias, void *conv_states,
+                                      const int32_t *cache_indices,
+                                      const uint8_t *has_initial_state,
+                                      const int32_t *query_start_loc, int64_t num_seqs,
+                                      int64_t null_block_id, int activation, void *out,
+                                      const kda_conv_layout_t *layout, const kda_l2norm_t *norm,
+                                      kda_stream_t stream);
+
+/*
+ * kda_conv1d_update_l2norm -- kda_conv1d_update with the same L2 norm: the
+ * decode step's q and k rows leave normalised, as in the fused decode kernel
+ * of the vLLM page "vllm.models.kimi_k3.amd.ops.kda_decode".
+ */
+kda_status_t kda_conv1d_update_l2norm(const void *x, int64_t x_row_stride, int64_t batch,
+                                      int64_t dim, int64_t part_dim, const float *weight,
+                                      const float *bias, void *conv_states,
+                                      const int32_t *cache_indices, int64_t null_block_id,
+                                      int activation, void *out, const kda_conv_layout_t *layout,
+                                      const kda_l2norm_t *norm, kda_stream_t stream);
+
+/* kda_l2norm_check -- host only: the status the *_l2norm entry points return
+ * for these norm options with this dim and part_dim. No CUDA call is made. */
+kda_status_t kda_l2norm_check(const kda_l2norm_t *norm, int64_t dim, int64_t part_dim);
+
+/*
  * kda_packed_conv1d_preact_f32 -- the same conv without activation or rounding:
  * `out` receives the FP32 accumulator (dim/part_dim, tokens, part_dim) and the conv
  * state is updated exactly as by kda_packed_conv1d. Same arguments and rules as

@@ -22,13 +22,18 @@ from ._binding import (  # noqa: F401
     KDA_OK,
     KdaConvLayout,
     KdaError,
+    KdaL2Norm,
     causal_conv1d_update,
     epilogue_range,
     kda_conv1d_update,
+    kda_conv1d_update_l2norm,
     kda_packed_conv1d,
     kda_packed_conv1d_ex,
+    kda_packed_conv1d_l2norm,
     kda_packed_conv1d_preact_f32,
+    l2norm_check,
     layout_of,
+    make_l2norm,
     make_layout,
     launch_shape,
     lib,

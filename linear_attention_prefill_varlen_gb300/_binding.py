@@ -49,6 +49,17 @@ def make_layout(x_dtype: int, state_width: int, state_stride, weight_stride,
                          (ctypes.c_int64 * 2)(*weight_stride), state_dtype, 0)
 
 
+class KdaL2Norm(ctypes.Structure):
+    """kda_l2norm_t: planes to normalise per head, head size, epsilon."""
+
+    _fields_ = [("plane_mask", ctypes.c_uint32), ("head_dim", ctypes.c_int32),
+                ("eps", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
+def make_l2norm(plane_mask: int, head_dim: int = 128, eps: float = 1e-6) -> KdaL2Norm:
+    return KdaL2Norm(plane_mask, head_dim, eps, 0)
+
+
 def lib_path() -> str:
     return _build.LIB_PATH
 
@@ -61,6 +72,12 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     handle.kda_packed_conv1d_ex.argtypes = conv + [C, P, ctypes.POINTER(KdaConvLayout), P]
     handle.kda_conv1d_update.argtypes = [P, I64, I64, I64, I64, P, P, P, P, I64, C, P,
                                          ctypes.POINTER(KdaConvLayout), P]
+    handle.kda_packed_conv1d_l2norm.argtypes = conv + [C, P, ctypes.POINTER(KdaConvLayout),
+                                                       ctypes.POINTER(KdaL2Norm), P]
+    handle.kda_conv1d_update_l2norm.argtypes = [P, I64, I64, I64, I64, P, P, P, P, I64, C, P,
+                                                ctypes.POINTER(KdaConvLayout),
+                                                ctypes.POINTER(KdaL2Norm), P]
+    handle.kda_l2norm_check.argtypes = [ctypes.POINTER(KdaL2Norm), I64, I64]
     handle.kda_packed_conv1d_ex_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P,
                                                        I64, C, P, ctypes.POINTER(KdaConvLayout)]
     handle.kda_packed_conv1d_check_args.argtypes = [P, I64, I64, I64, I64, P, P, P, P, P, P, I64,
@@ -71,7 +88,8 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     handle.kda_validate_metadata.argtypes = [P, P, I64, I64, I64, I64, ctypes.POINTER(I64)]
     handle.kda_epilogue_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, C, P, P]
     for name in ("kda_packed_conv1d", "kda_packed_conv1d_preact_f32", "kda_packed_conv1d_ex",
-                 "kda_conv1d_update",
+                 "kda_conv1d_update", "kda_packed_conv1d_l2norm", "kda_conv1d_update_l2norm",
+                 "kda_l2norm_check",
                  "kda_packed_conv1d_ex_check_args",
                  "kda_packed_conv1d_check_args", "kda_packed_conv1d_launch_shape",
                  "kda_validate_metadata", "kda_epilogue_range"):
@@ -158,13 +176,49 @@ def kda_conv1d_update(x, x_row_stride: int, batch: int, dim: int, part_dim: int,
         None if layout is None else ctypes.byref(layout), _stream(stream)))
 
 
+def _byref(s):
+    return None if s is None else ctypes.byref(s)
+
+
+def kda_packed_conv1d_l2norm(x, x_row_stride: int, tokens: int, dim: int, part_dim: int,
+                             weight, bias, conv_states, cache_indices, has_initial_state,
+                             query_start_loc, num_seqs: int, null_block_id: int,
+                             activation: int, out, layout: KdaConvLayout | None,
+                             norm: KdaL2Norm | None, stream=None) -> None:
+    """C-ABI kda_packed_conv1d_l2norm (norm None: kda_packed_conv1d_ex)."""
+    _check(lib().kda_packed_conv1d_l2norm(
+        _ptr(x), x_row_stride, tokens, dim, part_dim, _ptr(weight), _ptr(bias),
+        _ptr(conv_states), _ptr(cache_indices), _ptr(has_initial_state), _ptr(query_start_loc),
+        num_seqs, null_block_id, activation, _ptr(out), _byref(layout), _byref(norm),
+        _stream(stream)))
+
+
+def kda_conv1d_update_l2norm(x, x_row_stride: int, batch: int, dim: int, part_dim: int,
+                             weight, bias, conv_states, cache_indices, null_block_id: int,
+                             activation: int, out, layout: KdaConvLayout | None,
+                             norm: KdaL2Norm | None, stream=None) -> None:
+    """C-ABI kda_conv1d_update_l2norm (norm None: kda_conv1d_update)."""
+    _check(lib().kda_conv1d_update_l2norm(
+        _ptr(x), x_row_stride, batch, dim, part_dim, _ptr(weight), _ptr(bias), _ptr(conv_states),
+        _ptr(cache_indices), null_block_id, activation, _ptr(out), _byref(layout), _byref(norm),
+        _stream(stream)))
+
+
+def l2norm_check(norm: KdaL2Norm | None, dim: int, part_dim: int) -> int:
+    """Host-only status of these norm options (no CUDA call)."""
+    return lib().kda_l2norm_check(_byref(norm), dim, part_dim)
+
+
 def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: torch.Tensor,
                          bias: torch.Tensor | None, cache_indices: torch.Tensor, part_dim: int,
                          activation="silu", null_block_id: int | None = None,
-                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                         out: torch.Tensor | None = None, stream=None,
+                         use_qk_l2norm: bool = False, head_dim: int = 128,
+                         l2norm_eps: float = 1e-6) -> torch.Tensor:
     """One decode step: x (batch, dim), row i the next token of the sequence at
     conv-state line cache_indices[i].  Returns (dim // part_dim, batch, part_dim)
-    in x's dtype and shifts each touched line by one row, in place."""
+    in x's dtype and shifts each touched line by one row, in place.
+    `use_qk_l2norm` as for packed_causal_conv1d_fn."""
     batch, dim = x.shape
     if out is None:
         out = torch.empty((dim // part_dim, batch, part_dim), dtype=x.dtype, device=x.device)
@@ -172,8 +226,10 @@ def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: tor
         raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
     act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
-    kda_conv1d_update(x, x.stride(0), batch, dim, part_dim, weight, bias, conv_states,
-                      cache_indices, null, act, out, layout_of(x, weight, conv_states), stream)
+    norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
+    kda_conv1d_update_l2norm(x, x.stride(0), batch, dim, part_dim, weight, bias, conv_states,
+                             cache_indices, null, act, out, layout_of(x, weight, conv_states),
+                             norm, stream)
     return out
 
 
@@ -275,14 +331,17 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
                             conv_states: torch.Tensor, query_start_loc: torch.Tensor,
                             cache_indices: torch.Tensor, has_initial_state: torch.Tensor,
                             part_dim: int, activation="silu", null_block_id: int | None = None,
-                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                            out: torch.Tensor | None = None, stream=None,
+                            use_qk_l2norm: bool = False, head_dim: int = 128,
+                            l2norm_eps: float = 1e-6) -> torch.Tensor:
     """Varlen causal depthwise conv of x (tokens, dim), dim = parts x part_dim.
 
     Returns (dim // part_dim, tokens, part_dim) in x's dtype; conv_states is
     updated in place.  `activation` in ("silu", "swish", True) selects SiLU,
     anything else none.  `null_block_id=None` disables padding detection (the
     library gets a value no cache index can hold).  `out` may be given to
-    avoid the allocation."""
+    avoid the allocation.  `use_qk_l2norm` normalises each head_dim-channel
+    head of planes 0 and 1 (q and k) per token, y / sqrt(sum y^2 + l2norm_eps)."""
     tokens, dim = x.shape
     num_seqs = query_start_loc.numel() - 1
     if out is None:
@@ -293,7 +352,9 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
         raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
     act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
-    kda_packed_conv1d_ex(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
-                         cache_indices, has_initial_state, query_start_loc, max(num_seqs, 0),
-                         null, act, out, layout_of(x, weight, conv_states), stream)
+    norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
+    kda_packed_conv1d_l2norm(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
+                             cache_indices, has_initial_state, query_start_loc,
+                             max(num_seqs, 0), null, act, out, layout_of(x, weight, conv_states),
+                             norm, stream)
     return out

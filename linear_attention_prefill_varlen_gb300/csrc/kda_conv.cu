@@ -113,6 +113,9 @@ struct Params {
     int64_t total_warps;   // programs * warps_per_prog
     int search_steps;      // radix-32 levels: smallest s with 32^s >= num_seqs
     int search_top;        // 32^(search_steps - 1)
+    uint32_t norm_mask;    // planes whose heads are L2-normalised (kNorm kernels)
+    int norm_lanes;        // lanes per head: head_dim / VEC (a power of two <= 32)
+    float norm_eps;        // added to the sum of squares inside the root
 };
 
 // ---------------------------------------------------------------------------
@@ -336,6 +339,63 @@ __device__ __forceinline__ void silu_row(float (&y)[VEC]) {
     for (int v = 0; v < VEC; ++v) y[v] = silu_f32(y[v]);
 }
 
+// 1/sqrt(x) on the special-function unit (PTX rsqrt.approx.ftz: relative
+// error about 2^-23; subnormal inputs are flushed to 0, giving +inf).
+__device__ __forceinline__ float rsqrt_approx(float x) {
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The q/k L2 norm of G rows: a head is `lanes` consecutive lanes' VEC
+// channels (lanes a power of two, the group aligned), all of which call this
+// together with the group's lane mask.  Each row y *= 1 / sqrt(sum of y^2 +
+// eps): the sum in FP32 (each lane's squares, then a butterfly over the
+// group, unrolled for the 32-lane head of 128 channels), the root on the
+// SFU.  The G butterflies are independent, so their shuffles overlap instead
+// of waiting on one another.
+template <int G, int VEC>
+__device__ __forceinline__ void l2norm_rows(float (&y)[G][VEC], float eps, int lanes,
+                                            unsigned mask) {
+    float ss[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        ss[g] = 0.0f;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) ss[g] = __fmaf_rn(y[g][v], y[g][v], ss[g]);
+    }
+    if (lanes == 32) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) ss[g] += __shfl_xor_sync(0xFFFFFFFFu, ss[g], off);
+        }
+    } else {
+        for (int off = lanes >> 1; off > 0; off >>= 1) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) ss[g] += __shfl_xor_sync(mask, ss[g], off);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float r = rsqrt_approx(ss[g] + eps);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) y[g][v] *= r;
+    }
+}
+
+template <int VEC>
+__device__ __forceinline__ void l2norm_row(float (&y)[VEC], float eps, int lanes,
+                                           unsigned mask) {
+    l2norm_rows<1, VEC>(reinterpret_cast<float (&)[1][VEC]>(y), eps, lanes, mask);
+}
+
+// The lane mask of this lane's head group (`lanes` a power of two <= 32).
+__device__ __forceinline__ unsigned head_group_mask(int lane, int lanes) {
+    if (lanes >= 32) return 0xFFFFFFFFu;
+    return ((1u << lanes) - 1u) << (lane & ~(lanes - 1));
+}
+
 // The sequence that owns program `prog`, or -1 if the program is idle before
 // the first sequence.  Must be called by all 32 lanes of a warp.
 __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane) {
@@ -358,10 +418,13 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
 // ---------------------------------------------------------------------------
 
 // Resident CTAs per SM the register budget is sized for: fp32 rows are twice
-// as wide, so their queue needs more registers.
-template <int kDtype>
+// as wide, so their queue needs more registers.  The L2-norm epilogue holds a
+// whole step's activations at once (its P head reductions run side by side),
+// which costs two CTAs.  Measured on GB300 for the 16K prefill with the norm:
+// 6 CTAs and one row at a time 68.5 us, 5 CTAs and all P rows 59.1 us.
+template <int kDtype, bool kNorm = false>
 __host__ __device__ constexpr int min_blocks() {
-    return kDtype == KDA_DTYPE_F32 ? KDA_MIN_BLOCKS_F32 : KDA_MIN_BLOCKS;
+    return (kDtype == KDA_DTYPE_F32 ? KDA_MIN_BLOCKS_F32 : KDA_MIN_BLOCKS) - (kNorm ? 2 : 0);
 }
 
 // kGeneral: the weight and the conv state may have any strides and the state
@@ -371,9 +434,10 @@ __host__ __device__ constexpr int min_blocks() {
 // batches of short sequences: its mere presence costs the long-chunk path
 // about 3 % on GB300 (register allocation and scheduling of the main loop
 // shift), while it saves 10-15 % on batches of one- to five-token sequences.
+// kNorm: planes in norm_mask get the per-head L2 norm after the activation.
 template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias,
-          bool kShort>
-__global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
+          bool kShort, bool kNorm>
+__global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>()))
     kda_packed_conv1d_kernel(const Params p) {
 #if KDA_PDL
     // Launched as a programmatic dependent: wait until the preceding grid in
@@ -537,6 +601,9 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
     const int plane = c / p.part_dim;
     const int col = c - plane * p.part_dim;
     const int64_t out_row = p.part_dim;  // elements between output rows
+    // Heads never straddle planes, so a head group agrees on norm_on.
+    const bool norm_on = kNorm && ((p.norm_mask >> plane) & 1u);
+    const unsigned norm_group = kNorm ? head_group_mask(lane, p.norm_lanes) : 0u;
     int64_t o = (int64_t)plane * p.plane_stride + col + (int64_t)t0 * out_row;
     const XT *xnext = xcol + (int64_t)(t0 + P) * xs;
 
@@ -545,6 +612,39 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
     int t = t0;
     auto rows = [&](auto checked_tag) {
         constexpr bool kChecked = decltype(checked_tag)::value;
+        if constexpr (kNorm) {
+            // The step's P activations first, then their P head reductions
+            // side by side, then the stores.
+            float y[P][VEC];
+#pragma unroll
+            for (int u = 0; u < P; ++u) {
+                float xv[VEC];
+                widen<VEC, kDtype>(q[u], xv);
+                if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) {
+                    float acc = kBias ? bias[v] : 0.0f;
+                    acc = __fmaf_rn(h0[v], w[v][0], acc);
+                    acc = __fmaf_rn(h1[v], w[v][1], acc);
+                    acc = __fmaf_rn(h2[v], w[v][2], acc);
+                    acc = __fmaf_rn(xv[v], w[v][3], acc);
+                    y[u][v] = acc;
+                    h0[v] = h1[v];
+                    h1[v] = h2[v];
+                    h2[v] = xv[v];
+                }
+                if constexpr (kSilu) silu_row<VEC>(y[u]);
+            }
+            if (norm_on) l2norm_rows<P, VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
+#pragma unroll
+            for (int u = 0; u < P; ++u) {
+                if (!kChecked || t + u < t1)
+                    store_out_row<VEC, kDtype>(static_cast<OT *>(p.out) + o + u * out_row, y[u]);
+            }
+            xnext += P * xs;
+            o += P * out_row;
+            return;
+        }
 #pragma unroll
         for (int u = 0; u < P; ++u) {
             float xv[VEC];
@@ -599,6 +699,9 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, min_blocks<kDtype>())
                     h2[v] = xv[v];
                 }
                 if constexpr (kSilu) silu_row<VEC>(y);
+                if constexpr (kNorm) {
+                    if (norm_on) l2norm_row<VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
+                }
                 OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
                 if constexpr (kPreact)
                     store_f32_row<VEC>(dst, y);
@@ -646,7 +749,7 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 
 // kLayout: 0 dense weight and dense fp32 state; 1 dense weight and dense bf16
 // state; 2 any strides, width and state type (kGeneral).
-template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias>
+template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
 __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     kda_conv1d_update_kernel(const Params p) {
     constexpr bool kGeneral = kLayout == 2;
@@ -758,6 +861,13 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     }
     if constexpr (kSilu) silu_row<VEC>(y);
     const int plane = c / p.part_dim;
+    if constexpr (kNorm) {
+        // A head group is `norm_lanes` consecutive threads of one token (dim is
+        // a multiple of head_dim), so the group exits or stays together above.
+        if ((p.norm_mask >> plane) & 1u)
+            l2norm_row<VEC>(y, p.norm_eps, p.norm_lanes,
+                            head_group_mask(threadIdx.x & 31, p.norm_lanes));
+    }
     const int col = c - plane * p.part_dim;
     store_out_row<VEC, kDtype>(
         static_cast<XT *>(p.out) + (int64_t)plane * p.plane_stride + token * p.part_dim + col, y);
@@ -931,16 +1041,27 @@ void launch_kernel(void (*kernel)(Params), unsigned blocks, unsigned threads, co
 #endif
 }
 
+template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias, bool kNorm>
+void launch_norm(const Params &p, const Shape &sh, cudaStream_t stream) {
+    if (sh.short_seqs)
+        launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu,
+                                               kBias, true, kNorm>,
+                      (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+    else
+        launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu,
+                                               kBias, false, kNorm>,
+                      (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+}
+
 template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
 void launch(const Params &p, const Shape &sh, cudaStream_t stream) {
-    if (sh.short_seqs)
-        launch_kernel(
-            kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias, true>,
-            (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
-    else
-        launch_kernel(
-            kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu, kBias, false>,
-            (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+    if constexpr (!kPreact) {
+        if (p.norm_mask != 0u) {
+            launch_norm<kDtype, kGeneral, kPreact, kSilu, kBias, true>(p, sh, stream);
+            return;
+        }
+    }
+    launch_norm<kDtype, kGeneral, kPreact, kSilu, kBias, false>(p, sh, stream);
 }
 
 template <int kDtype, bool kGeneral>
@@ -978,21 +1099,48 @@ kda_status_t record_cuda_error() {
     return KDA_OK;
 }
 
+// The L2-norm options: NULL or an empty mask is no norm.  A head is head_dim
+// channels, head_dim / kVec lanes: a power of two up to a warp, dividing
+// part_dim so that heads never straddle planes.
+kda_status_t check_norm(const kda_l2norm_t *norm, int64_t dim, int64_t part_dim) {
+    if (!norm || norm->plane_mask == 0u) return KDA_OK;
+    if (norm->reserved != 0) return KDA_ERR_INVALID_ARG;
+    if (!(norm->eps >= 0.0f) || norm->eps > 3.0e38f) return KDA_ERR_INVALID_ARG;  // NaN too
+    const int64_t planes = dim / part_dim;
+    if (planes < 32 && (norm->plane_mask >> planes) != 0u) return KDA_ERR_INVALID_ARG;
+    const int64_t hd = norm->head_dim;
+    if (hd < kVec || hd % kVec != 0) return KDA_ERR_UNSUPPORTED;
+    const int64_t lanes = hd / kVec;
+    if (lanes > 32 || (lanes & (lanes - 1)) != 0) return KDA_ERR_UNSUPPORTED;
+    if (part_dim % hd != 0) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+void set_norm(Params &p, const kda_l2norm_t *norm) {
+    const bool on = norm && norm->plane_mask != 0u;
+    p.norm_mask = on ? norm->plane_mask : 0u;
+    p.norm_lanes = on ? norm->head_dim / kVec : 1;
+    p.norm_eps = on ? norm->eps : 0.0f;
+}
+
 kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
                  int64_t part_dim, const float *weight, const float *bias, void *conv_states,
                  const int32_t *cache_indices, const uint8_t *has_initial_state,
                  const int32_t *query_start_loc, int64_t num_seqs, int64_t null_block_id,
                  int activation, void *out, bool preact, const kda_conv_layout_t *layout,
-                 kda_stream_t stream) {
+                 const kda_l2norm_t *norm, kda_stream_t stream) {
     const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
     kda_status_t st = check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
                                  cache_indices, has_initial_state, query_start_loc, num_seqs,
                                  activation, out, l);
     if (st != KDA_OK) return st;
+    if (part_dim > 0 && (st = check_norm(norm, dim, part_dim)) != KDA_OK) return st;
     if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;
 
+    const bool norm_on = !preact && norm && norm->plane_mask != 0u;
     const int blocks_per_sm =
-        l.x_dtype == KDA_DTYPE_F32 ? min_blocks<KDA_DTYPE_F32>() : min_blocks<KDA_DTYPE_BF16>();
+        (l.x_dtype == KDA_DTYPE_F32 ? min_blocks<KDA_DTYPE_F32>() : min_blocks<KDA_DTYPE_BF16>()) -
+        (norm_on ? 2 : 0);
     const Shape sh = launch_shape(tokens, dim, num_seqs, current_sms(), blocks_per_sm);
     if (sh.ctas > INT32_MAX) return KDA_ERR_INVALID_ARG;
     Params p;
@@ -1029,6 +1177,7 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     }
     p.search_steps = steps;
     p.search_top = steps > 0 ? (int)(reach / 32) : 1;
+    set_norm(p, preact ? nullptr : norm);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (preact) {  // bf16 x and the default layout only
@@ -1048,8 +1197,12 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
 
 template <int kDtype, int kLayout, bool kSilu, bool kBias>
 void launch_update(const Params &p, int64_t blocks, cudaStream_t stream) {
-    launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias>,
-                  (unsigned)blocks, 256, p, stream);
+    if (p.norm_mask != 0u)
+        launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias, true>,
+                      (unsigned)blocks, 256, p, stream);
+    else
+        launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias, false>,
+                      (unsigned)blocks, 256, p, stream);
 }
 
 template <int kDtype, int kLayout>
@@ -1084,12 +1237,13 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
                         int64_t part_dim, const float *weight, const float *bias,
                         void *conv_states, const int32_t *cache_indices, int64_t null_block_id,
                         int activation, void *out, const kda_conv_layout_t *layout,
-                        kda_stream_t stream) {
+                        const kda_l2norm_t *norm, kda_stream_t stream) {
     const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
     kda_status_t st = check_args(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
                                  cache_indices, nullptr, nullptr, batch, activation, out, l,
                                  false);
     if (st != KDA_OK) return st;
+    if (part_dim > 0 && (st = check_norm(norm, dim, part_dim)) != KDA_OK) return st;
     if (batch == 0 || dim == 0) return KDA_OK;
     const int64_t threads_total = batch * (dim / kVec);
     const int64_t blocks = (threads_total + 255) / 256;
@@ -1115,6 +1269,7 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     p.null_block_id = null_block_id;
     p.out = out;
     p.plane_stride = batch * part_dim;
+    set_norm(p, norm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool silu = activation == KDA_ACT_SILU;
     if (l.x_dtype == KDA_DTYPE_F16)
@@ -1138,7 +1293,7 @@ kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t toke
                                kda_stream_t stream) {
     return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
                has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
-               false, nullptr, stream);
+               false, nullptr, nullptr, stream);
 }
 
 kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t tokens,
@@ -1150,7 +1305,21 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
                                   const kda_conv_layout_t *layout, kda_stream_t stream) {
     return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
                has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
-               false, layout, stream);
+               false, layout, nullptr, stream);
+}
+
+kda_status_t kda_packed_conv1d_l2norm(const void *x, int64_t x_row_stride, int64_t tokens,
+                                      int64_t dim, int64_t part_dim, const float *weight,
+                                      const float *bias, void *conv_states,
+                                      const int32_t *cache_indices,
+                                      const uint8_t *has_initial_state,
+                                      const int32_t *query_start_loc, int64_t num_seqs,
+                                      int64_t null_block_id, int activation, void *out,
+                                      const kda_conv_layout_t *layout, const kda_l2norm_t *norm,
+                                      kda_stream_t stream) {
+    return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
+               has_initial_state, query_start_loc, num_seqs, null_block_id, activation, out,
+               false, layout, norm, stream);
 }
 
 kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
@@ -1159,7 +1328,17 @@ kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batc
                               int64_t null_block_id, int activation, void *out,
                               const kda_conv_layout_t *layout, kda_stream_t stream) {
     return run_update(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
-                      cache_indices, null_block_id, activation, out, layout, stream);
+                      cache_indices, null_block_id, activation, out, layout, nullptr, stream);
+}
+
+kda_status_t kda_conv1d_update_l2norm(const void *x, int64_t x_row_stride, int64_t batch,
+                                      int64_t dim, int64_t part_dim, const float *weight,
+                                      const float *bias, void *conv_states,
+                                      const int32_t *cache_indices, int64_t null_block_id,
+                                      int activation, void *out, const kda_conv_layout_t *layout,
+                                      const kda_l2norm_t *norm, kda_stream_t stream) {
+    return run_update(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
+                      cache_indices, null_block_id, activation, out, layout, norm, stream);
 }
 
 kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, int64_t tokens,
@@ -1171,7 +1350,7 @@ kda_status_t kda_packed_conv1d_preact_f32(const void *x, int64_t x_row_stride, i
                                           int64_t null_block_id, float *out, kda_stream_t stream) {
     return run(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states, cache_indices,
                has_initial_state, query_start_loc, num_seqs, null_block_id, KDA_ACT_NONE, out,
-               true, nullptr, stream);
+               true, nullptr, nullptr, stream);
 }
 
 kda_status_t kda_packed_conv1d_check_args(const void *x, int64_t x_row_stride, int64_t tokens,
@@ -1195,6 +1374,12 @@ kda_status_t kda_packed_conv1d_ex_check_args(
     return check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
                       cache_indices, has_initial_state, query_start_loc, num_seqs, activation,
                       out, layout ? *layout : default_layout(dim));
+}
+
+kda_status_t kda_l2norm_check(const kda_l2norm_t *norm, int64_t dim, int64_t part_dim) {
+    kda_status_t st = check_sizes(dim, 0, dim, part_dim, 0);
+    if (st != KDA_OK) return st;
+    return check_norm(norm, dim, part_dim);
 }
 
 kda_status_t kda_packed_conv1d_launch_shape(int64_t tokens, int64_t dim, int64_t part_dim,

@@ -388,9 +388,9 @@ int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int
 /*
  * The q/k L2 norm, per token and head.  "vllm.models.kimi_k3.amd.ops.
  * kda_prefill" (chunk_kda_prefill: q and k are [1, T, H, K]; its
- * use_qk_l2norm_in_kernel parameter folds "the q/k L2 norm" into the kernel,
- * and the fused path's comment says its prologue takes over that norm) norms
- * each head's K channels of a token.  The pages print neither the formula's
+ * use_qk_l2norm_in_kernel flag moves the normalisation of q and k into the
+ * kernel that consumes them, and the fused path's comment gives it to that
+ * kernel's prologue) norms each head's K channels of a token.  The pages print neither the formula's
  * epsilon nor its precision.  The reading: out = y / sqrt(sum over the head
  * of y^2 + eps), eps a caller argument, computed here in double from the FP32
  * conv outputs y (after the activation).

@@ -236,3 +236,36 @@ def test_supported_predicate_rejects_host_tensors(kda):
     w = torch.zeros(128, 4)
     st = torch.zeros(2, 128, 3)
     assert not kda.packed_causal_conv1d_supported(x, w, st, 64)
+
+
+@pytest.mark.parametrize("mask,head_dim,eps,dim,part_dim,status", [
+    (0b011, 128, 1e-6, 4608, 1536, 0),
+    (0b011, 64, 1e-6, 3264, 1088, 0),
+    (0b011, 128, 1e-6, 3264, 1088, 2),  # 1088 is not a multiple of 128
+    (0b111, 4, 0.0, 4608, 1536, 0),
+    (0b1000, 128, 1e-6, 4608, 1536, 1),  # plane 3 of 3
+    (0b011, 96, 1e-6, 4608, 1536, 2),  # 24 lanes: not a power of two
+    (0b011, 256, 1e-6, 4608, 1536, 2),  # more than a warp
+    (0b011, 2, 1e-6, 4608, 1536, 2),  # less than one lane's channels
+    (0b011, 128, -1e-6, 4608, 1536, 1),
+    (0b011, 128, float("nan"), 4608, 1536, 1),
+    (0b011, 128, float("inf"), 4608, 1536, 1),
+    (0, 7, -5.0, 4608, 1536, 0),  # empty mask: no norm, nothing else checked
+])
+def test_l2norm_checks(kda, mask, head_dim, eps, dim, part_dim, status):
+    assert kda.l2norm_check(kda.make_l2norm(mask, head_dim, eps), dim, part_dim) == status
+
+
+def test_l2norm_reserved_and_null(kda):
+    norm = kda.make_l2norm(0b011, 128, 1e-6)
+    norm.reserved = 1
+    assert kda.l2norm_check(norm, 4608, 1536) == 1
+    assert kda.l2norm_check(None, 4608, 1536) == 0
+    assert kda.l2norm_check(kda.make_l2norm(1, 64, 0.0), 4608, 0) == 1  # bad sizes first
+
+
+def test_l2norm_struct_matches_the_header(kda):
+    import ctypes
+
+    assert ctypes.sizeof(kda.KdaL2Norm) == 16
+    assert kda.KdaL2Norm.eps.offset == 8
