@@ -560,7 +560,8 @@ def run_ours(args) -> None:
     achieved = nbytes / (ms_per_step * 1e-3) / 1e9
     extra = {
         "vs_baseline": (round(value / world / PAGE_GBS, 4)
-                        if ENTRY == "packed" and b.name in PAGE_WORKLOADS else None),
+                        if ENTRY == "packed" and NORM is None and b.name in PAGE_WORKLOADS
+                        else None),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(ENTRY, b.name), "peak_source": peak_kind,
