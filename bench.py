@@ -344,6 +344,30 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
             "clocks": clocks.summary()}
 
 
+def time_graph(pkg, b: workloads.Batch, sets: list, launches: int, dev) -> float:
+    """The same launches captured in one CUDA graph (rotating over the sets)
+    and replayed: microseconds per launch over one timed replay, after one
+    untimed replay.  Outside the timed region of the bench step."""
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        call(pkg, b, sets[0], stream.cuda_stream)  # first use outside capture
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        cur = torch.cuda.current_stream().cuda_stream
+        for i in range(launches):
+            call(pkg, b, sets[i % len(sets)], cur)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * 1e3 / launches
+
+
 def time_e2e(pkg, b: workloads.Batch, steps: int, dev) -> dict:
     """The same call with HOST inputs and result.  Every step copies its x
     (the (tokens, dim) slice) and metadata from pinned host memory, runs the
@@ -547,6 +571,9 @@ def run_ours(args) -> None:
     t = time_device(pkg, b, sets, args.steps, args.warmup, dist, dev, flush)
     ms_per_step, value = aggregate(dist, world, nbytes, t["step_ms_total"], args.steps, dev)
     iso_median = dist.max(statistics.median(t["iso_ms"]), dev)
+    graph_us = None
+    if flush is None:  # back-to-back timing only: a flush cannot live inside the graph
+        graph_us = dist.max(time_graph(pkg, b, sets, min(args.steps, 500), dev), dev)
     iso_min = dist.max(min(t["iso_ms"]), dev)
 
     e2e = time_e2e(pkg, b, args.e2e_steps, dev)
@@ -570,6 +597,7 @@ def run_ours(args) -> None:
                      "launch_us_mean": round(ms_per_step * 1e3, 3),
                      "launch_us_isolated_median": round(iso_median * 1e3, 3),
                      "launch_us_isolated_min": round(iso_min * 1e3, 3),
+                     "launch_us_graph_replay": None if graph_us is None else round(graph_us, 3),
                      "timing": ("back-to-back launches, region events / K" if flush is None else
                                 "per-launch events after an L2 flush")},
         "e2e": {"value": round(world * nbytes / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
