@@ -306,6 +306,27 @@ __device__ __forceinline__ void state_set(const Params &p, int64_t i, float v) {
         static_cast<float *>(p.conv_states)[i] = v;
 }
 
+// One row's four taps per channel, oldest first, from the accumulator's start
+// value (the bias, or +0 without one) with fused multiply-adds; then the
+// history moves up a row (h0 <- h1 <- h2 <- x).
+template <int VEC, bool kBias>
+__device__ __forceinline__ void taps_row(const float (&w)[VEC][4], const float (&bias)[VEC],
+                                         float (&h0)[VEC], float (&h1)[VEC], float (&h2)[VEC],
+                                         const float (&xv)[VEC], float (&y)[VEC]) {
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+        float acc = kBias ? bias[v] : 0.0f;
+        acc = __fmaf_rn(h0[v], w[v][0], acc);
+        acc = __fmaf_rn(h1[v], w[v][1], acc);
+        acc = __fmaf_rn(h2[v], w[v][2], acc);
+        acc = __fmaf_rn(xv[v], w[v][3], acc);
+        y[v] = acc;
+        h0[v] = h1[v];
+        h1[v] = h2[v];
+        h2[v] = xv[v];
+    }
+}
+
 // 2^x and 1/x on the special-function unit (PTX ex2.approx.ftz / rcp.approx.ftz:
 // relative error about 2^-22; subnormal inputs and results are flushed to 0).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -621,18 +642,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
                 float xv[VEC];
                 widen<VEC, kDtype>(q[u], xv);
                 if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) {
-                    float acc = kBias ? bias[v] : 0.0f;
-                    acc = __fmaf_rn(h0[v], w[v][0], acc);
-                    acc = __fmaf_rn(h1[v], w[v][1], acc);
-                    acc = __fmaf_rn(h2[v], w[v][2], acc);
-                    acc = __fmaf_rn(xv[v], w[v][3], acc);
-                    y[u][v] = acc;
-                    h0[v] = h1[v];
-                    h1[v] = h2[v];
-                    h2[v] = xv[v];
-                }
+                taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y[u]);
                 if constexpr (kSilu) silu_row<VEC>(y[u]);
             }
             if (norm_on) l2norm_rows<P, VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
@@ -651,18 +661,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
             widen<VEC, kDtype>(q[u], xv);
             if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
             float y[VEC];
-#pragma unroll
-            for (int v = 0; v < VEC; ++v) {
-                float acc = kBias ? bias[v] : 0.0f;
-                acc = __fmaf_rn(h0[v], w[v][0], acc);
-                acc = __fmaf_rn(h1[v], w[v][1], acc);
-                acc = __fmaf_rn(h2[v], w[v][2], acc);
-                acc = __fmaf_rn(xv[v], w[v][3], acc);
-                y[v] = acc;
-                h0[v] = h1[v];
-                h1[v] = h2[v];
-                h2[v] = xv[v];
-            }
+            taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);
             if constexpr (kSilu) silu_row<VEC>(y);
             if (!kChecked || t + u < t1) {
                 OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
@@ -686,18 +685,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
                 float xv[VEC];
                 widen<VEC, kDtype>(q[u], xv);
                 float y[VEC];
-#pragma unroll
-                for (int v = 0; v < VEC; ++v) {
-                    float acc = kBias ? bias[v] : 0.0f;
-                    acc = __fmaf_rn(h0[v], w[v][0], acc);
-                    acc = __fmaf_rn(h1[v], w[v][1], acc);
-                    acc = __fmaf_rn(h2[v], w[v][2], acc);
-                    acc = __fmaf_rn(xv[v], w[v][3], acc);
-                    y[v] = acc;
-                    h0[v] = h1[v];
-                    h1[v] = h2[v];
-                    h2[v] = xv[v];
-                }
+                taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);
                 if constexpr (kSilu) silu_row<VEC>(y);
                 if constexpr (kNorm) {
                     if (norm_on) l2norm_row<VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
@@ -850,15 +838,7 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     }
 
     float y[VEC];
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) {
-        float acc = kBias ? bias[v] : 0.0f;
-        acc = __fmaf_rn(h0[v], w[v][0], acc);
-        acc = __fmaf_rn(h1[v], w[v][1], acc);
-        acc = __fmaf_rn(h2[v], w[v][2], acc);
-        acc = __fmaf_rn(xv[v], w[v][3], acc);
-        y[v] = acc;
-    }
+    taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);  // the history is not used after
     if constexpr (kSilu) silu_row<VEC>(y);
     const int plane = c / p.part_dim;
     if constexpr (kNorm) {
