@@ -405,6 +405,50 @@ __device__ __forceinline__ void l2norm_rows(float (&y)[G][VEC], float eps, int l
     }
 }
 
+// The same for up to 8 rows over a full-warp head (32 lanes), as a
+// reduce-scatter: three halving levels leave each lane with one row's partial
+// sum over 8 lanes (row 4*b4 + 2*b3 + b2 of its lane bits), two more levels
+// complete it, one reciprocal root per lane, and each row's factor is then
+// read from lane 4 * row.  Fewer shuffles and roots than G butterflies.
+template <int G, int VEC>
+__device__ __forceinline__ void l2norm_rows_warp(float (&y)[G][VEC], float eps, int lane) {
+    static_assert(G <= 8, "up to eight rows");
+    float s[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        s[g] = 0.0f;
+        if (g < G) {
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) s[g] = __fmaf_rn(y[g][v], y[g][v], s[g]);
+        }
+    }
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float k4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float keep = b4 ? s[4 + i] : s[i];
+        const float send = b4 ? s[i] : s[4 + i];
+        k4[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    }
+    float k2[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float keep = b3 ? k4[2 + i] : k4[i];
+        const float send = b3 ? k4[i] : k4[2 + i];
+        k2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    }
+    float k1 = (b2 ? k2[1] : k2[0]) + __shfl_xor_sync(0xFFFFFFFFu, b2 ? k2[0] : k2[1], 4);
+    k1 += __shfl_xor_sync(0xFFFFFFFFu, k1, 2);
+    k1 += __shfl_xor_sync(0xFFFFFFFFu, k1, 1);
+    const float r = rsqrt_approx(k1 + eps);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        const float rg = __shfl_sync(0xFFFFFFFFu, r, 4 * g);
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) y[g][v] *= rg;
+    }
+}
+
 template <int VEC>
 __device__ __forceinline__ void l2norm_row(float (&y)[VEC], float eps, int lanes,
                                            unsigned mask) {
@@ -442,7 +486,8 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
 // as wide, so their queue needs more registers.  The L2-norm epilogue holds a
 // whole step's activations at once (its P head reductions run side by side),
 // which costs two CTAs.  Measured on GB300 for the 16K prefill with the norm:
-// 6 CTAs and one row at a time 68.5 us, 5 CTAs and all P rows 59.1 us.
+// 6 CTAs and one row at a time 68.5 us, 5 CTAs and all P rows 59.1 us (56.8 us
+// with the reduce-scatter form for 128-channel heads).
 template <int kDtype, bool kNorm = false>
 __host__ __device__ constexpr int min_blocks() {
     return (kDtype == KDA_DTYPE_F32 ? KDA_MIN_BLOCKS_F32 : KDA_MIN_BLOCKS) - (kNorm ? 2 : 0);
@@ -645,30 +690,33 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
                 taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y[u]);
                 if constexpr (kSilu) silu_row<VEC>(y[u]);
             }
-            if (norm_on) l2norm_rows<P, VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
+            if (norm_on) {
+                if (p.norm_lanes == 32)  // a 128-channel head: one warp's row
+                    l2norm_rows_warp<P, VEC>(y, p.norm_eps, lane);
+                else
+                    l2norm_rows<P, VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
+            }
 #pragma unroll
             for (int u = 0; u < P; ++u) {
                 if (!kChecked || t + u < t1)
                     store_out_row<VEC, kDtype>(static_cast<OT *>(p.out) + o + u * out_row, y[u]);
             }
-            xnext += P * xs;
-            o += P * out_row;
-            return;
-        }
+        } else {
 #pragma unroll
-        for (int u = 0; u < P; ++u) {
-            float xv[VEC];
-            widen<VEC, kDtype>(q[u], xv);
-            if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
-            float y[VEC];
-            taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);
-            if constexpr (kSilu) silu_row<VEC>(y);
-            if (!kChecked || t + u < t1) {
-                OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
-                if constexpr (kPreact)
-                    store_f32_row<VEC>(dst, y);
-                else
-                    store_out_row<VEC, kDtype>(dst, y);
+            for (int u = 0; u < P; ++u) {
+                float xv[VEC];
+                widen<VEC, kDtype>(q[u], xv);
+                if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
+                float y[VEC];
+                taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);
+                if constexpr (kSilu) silu_row<VEC>(y);
+                if (!kChecked || t + u < t1) {
+                    OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
+                    if constexpr (kPreact)
+                        store_f32_row<VEC>(dst, y);
+                    else
+                        store_out_row<VEC, kDtype>(dst, y);
+                }
             }
         }
         xnext += P * xs;
