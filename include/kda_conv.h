@@ -37,10 +37,11 @@
  * stated; the conv calls are asynchronous on the given stream, allocate
  * nothing, never synchronise, and launch a kernel and grid that depend only on
  * the scalar arguments (so a captured launch replays correctly for new
- * metadata values of the same tokens / num_seqs). When tokens < 6 * num_seqs
- * (sequences averaging under six rows, such as speculative-decoding
- * verification) the packed entry points launch an instantiation with a
- * short-chunk path. Its results are the same bit for bit. The conv kernels are launched as
+ * metadata values of the same tokens / num_seqs). When tokens < 16 * num_seqs
+ * (sequences averaging under 16 rows, such as decode tokens mixed into a
+ * prefill batch, or speculative-decoding verification) the packed entry
+ * points launch an instantiation with a short-chunk path. Its results are the
+ * same bit for bit. The conv kernels are launched as
  * programmatic dependents of the preceding kernel in the stream: they may be
  * scheduled while it drains, but every thread first waits until it has
  * completed and its writes are visible, so ordering is that of a plain launch.

@@ -914,6 +914,11 @@ constexpr int kThreads = KDA_CTA_THREADS;
 constexpr int kDefaultSms = 152;              // GB300, for shape queries without a device
 constexpr int kMinChunk = 2 * KDA_QUEUE;
 constexpr int kMaxChunk = 2048;
+// Mean sequence length below which the kShort instantiation is launched.
+// Measured on GB300 (1024-sequence batches): one-token sequences mixed with
+// longer ones gain 3-5 % at 16, a batch of uniform 12-token sequences loses
+// 1.7 %, and long sequences keep the plain instantiation.
+constexpr int kShortMean = 16;
 
 bool aligned(const void *ptr, uintptr_t bytes) {
     return (reinterpret_cast<uintptr_t>(ptr) & (bytes - 1)) == 0;
@@ -990,7 +995,7 @@ struct Shape {
     int64_t programs;
     int warps_per_prog;
     int64_t total_warps;
-    bool short_seqs;  // mean sequence length below the queue depth: the kShort kernel
+    bool short_seqs;  // mean sequence length below kShortMean: the kShort kernel
 };
 
 // Chunk length.  The resident-warp budget is waves x SMs x warps per SM.
@@ -1020,7 +1025,7 @@ Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
     sh.chunk = (int)chunk;
     sh.programs = (tokens + sh.chunk - 1) / sh.chunk + num_seqs;
     sh.total_warps = sh.programs * sh.warps_per_prog;
-    sh.short_seqs = tokens < (int64_t)kQueue * num_seqs;
+    sh.short_seqs = tokens < (int64_t)kShortMean * num_seqs;
     const int64_t warps_per_cta = kThreads / 32;
     sh.ctas = (sh.total_warps + warps_per_cta - 1) / warps_per_cta;
     return sh;
