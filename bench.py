@@ -118,7 +118,8 @@ class ClockSampler:
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+             "clocks.mem,temperature.gpu")
 
     def __init__(self, device_index: int):
         self.device_index = device_index
@@ -157,7 +158,8 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+                extra = [float(p) for p in parts[9:11]] if len(parts) >= 11 else [None, None]
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9], *extra))
             except ValueError:
                 continue
         if not rows:
@@ -167,8 +169,12 @@ class ClockSampler:
         names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(1, 5) if r[2][i] == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": sm_max,
-                "reasons": reasons, "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": sm_max,
+               "reasons": reasons, "samples": len(rows)}
+        if all(r[3] is not None for r in loaded):
+            out["mem_mhz"] = statistics.median(r[3] for r in loaded)
+            out["temp_c_max"] = max(r[4] for r in loaded)
+        return out
 
 
 def dist_env() -> tuple[int, int, int]:
