@@ -65,6 +65,14 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--x-dtype", default="bf16", choices=["bf16", "f16", "f32"],
+                    help="storage of x and out (fp16 / fp32 go through kda_packed_conv1d_ex)")
+    ap.add_argument("--state-width", type=int, default=3, help="conv state positions K >= 3")
+    ap.add_argument("--state-layout", default="dense", choices=["dense", "position_major"],
+                    help="position_major: (lines, K, dim) memory viewed as (lines, dim, K)")
+    ap.add_argument("--weight-layout", default="channel_major",
+                    choices=["channel_major", "tap_major"],
+                    help="tap_major: (4, dim) memory viewed as (dim, 4)")
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="the *_l2norm entry points: planes 0 and 1 normalised per 128-channel "
                          "head (eps 1e-6); the cpu_baseline stays the plain conv oracle")
@@ -91,11 +99,14 @@ def kernel_sha() -> str:
     return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
+STORAGE_SUFFIX = ""  # e.g. "_f32" or "_k4_state-position_major": set by main()
+
+
 def profile_path(entry: str, workload: str) -> str:
     kernel = "kda_conv1d_update" if entry == "update" else "kda_packed_conv1d"
     if NORM is not None:
         kernel += "_l2norm"
-    return os.path.join(PROFILES, f"{kernel}_{workload}.md")
+    return os.path.join(PROFILES, f"{kernel}_{workload}{STORAGE_SUFFIX}.md")
 
 
 def recorded_traffic(entry: str, workload: str) -> int | None:
@@ -219,25 +230,49 @@ def aggregate(dist: Dist, world: int, nbytes_per_rank: int, region_ms: float, st
     return ms_per_step, world * nbytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
-def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
-    """Device copies of one batch.  dense_x stores x as (tokens, dim) contiguous."""
+LAYOUT_OPTS = {"state_layout": "dense", "weight_layout": "channel_major"}  # set by main()
+
+
+def x_host_array(b: workloads.Batch, dense_x: bool) -> np.ndarray:
+    """x as stored: 16-bit patterns as int16, fp32 as float32."""
     x_np = b.x_buf[:, b.col_offset:b.col_offset + b.dim] if dense_x else b.x_buf
-    x = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).to(dev)
-    if b.conv_states.dtype == np.uint16:  # bf16 bits
-        states = torch.from_numpy(b.conv_states.view(np.int16)).to(dev).view(torch.bfloat16)
+    x_np = np.ascontiguousarray(x_np)
+    return x_np if b.x_dtype == "f32" else x_np.view(np.int16)
+
+
+def out_dtype(b: workloads.Batch):
+    return torch.float32 if b.x_dtype == "f32" else torch.int16
+
+
+def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
+    """Device copies of one batch.  dense_x stores x as (tokens, dim) contiguous.
+    The conv state and the weight take the memory orders LAYOUT_OPTS names."""
+    x = torch.from_numpy(x_host_array(b, dense_x)).to(dev)
+    esz = 4 if b.x_dtype == "f32" else 2
+    st_np = b.conv_states
+    if LAYOUT_OPTS["state_layout"] == "position_major":
+        st_np = np.ascontiguousarray(st_np.transpose(0, 2, 1))
+    if st_np.dtype == np.uint16:  # bf16 bits
+        states = torch.from_numpy(st_np.view(np.int16)).to(dev).view(torch.bfloat16)
     else:
-        states = torch.from_numpy(b.conv_states).to(dev)
+        states = torch.from_numpy(st_np).to(dev)
+    if LAYOUT_OPTS["state_layout"] == "position_major":
+        states = states.transpose(1, 2)
+    if LAYOUT_OPTS["weight_layout"] == "tap_major":
+        weight = torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t()
+    else:
+        weight = torch.from_numpy(b.weight).to(dev)
     return {
         "x": x,
-        "x_ptr": x.data_ptr() + (0 if dense_x else 2 * b.col_offset),
+        "x_ptr": x.data_ptr() + (0 if dense_x else esz * b.col_offset),
         "x_row_stride": b.dim if dense_x else b.row_stride,
-        "weight": torch.from_numpy(b.weight).to(dev),
+        "weight": weight,
         "bias": None if b.bias is None else torch.from_numpy(b.bias).to(dev),
         "conv_states": states,
         "cache_indices": torch.from_numpy(b.cache_indices).to(dev),
         "has_initial_state": torch.from_numpy(b.has_initial_state).to(dev),
         "query_start_loc": torch.from_numpy(b.query_start_loc).to(dev),
-        "out": torch.empty((b.dim // b.part_dim, b.tokens, b.part_dim), dtype=torch.int16,
+        "out": torch.empty((b.dim // b.part_dim, b.tokens, b.part_dim), dtype=out_dtype(b),
                            device=dev),
     }
 
@@ -245,12 +280,28 @@ def upload(b: workloads.Batch, dev, dense_x: bool = False) -> dict:
 ENTRY = "packed"
 
 
-def state_layout(pkg, states: torch.Tensor):
-    """None (the default layout) for an fp32 state, else a bf16-state layout."""
-    if states.dtype != torch.bfloat16:
+def upload_probe(b: workloads.Batch) -> dict:
+    """Host stand-ins with the strides upload() gives, for layout decisions."""
+    st = torch.empty(b.conv_states.shape, dtype=torch.bfloat16 if b.conv_states.dtype == np.uint16
+                     else torch.float32)
+    if LAYOUT_OPTS["state_layout"] == "position_major":
+        st = torch.empty((st.shape[0], st.shape[2], st.shape[1]), dtype=st.dtype).transpose(1, 2)
+    w = torch.empty(4, b.dim).t() if LAYOUT_OPTS["weight_layout"] == "tap_major" else \
+        torch.empty(b.dim, 4)
+    return {"conv_states": st, "weight": w}
+
+
+def state_layout(pkg, b: workloads.Batch, s: dict):
+    """None for the default layout (bf16 x, a dense width-3 fp32 state, a
+    channel-major weight), else the kda_conv_layout_t of these tensors."""
+    st, w = s["conv_states"], s["weight"]
+    default = (b.x_dtype == "bf16" and st.dtype == torch.float32 and st.size(2) == 3
+               and st.is_contiguous() and tuple(w.stride()) == (4, 1))
+    if default:
         return None
-    return pkg.make_layout(pkg.KDA_DTYPE_BF16, states.size(2), states.stride(), (4, 1),
-                           pkg.KDA_DTYPE_BF16)
+    dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
+    sdt = pkg.KDA_DTYPE_BF16 if st.dtype == torch.bfloat16 else pkg.KDA_DTYPE_F32
+    return pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride(), sdt)
 
 
 NORM = None  # --qk-l2norm: planes 0 and 1 normalised per 128-channel head
@@ -258,9 +309,11 @@ NORM = None  # --qk-l2norm: planes 0 and 1 normalised per 128-channel head
 
 def call(pkg, b: workloads.Batch, s: dict, stream) -> None:
     if "layout" not in s:
-        s["layout"] = state_layout(pkg, s["conv_states"])
+        s["layout"] = state_layout(pkg, b, s)
     if NORM is not None:
         lay = s["layout"] or pkg.make_layout(pkg.KDA_DTYPE_BF16, 3, (3 * b.dim, 3, 1), (4, 1))
+        if ENTRY != "update" and s["layout"] is None:
+            lay = None
         if ENTRY == "update":
             pkg.kda_conv1d_update_l2norm(
                 s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim, s["weight"],
@@ -380,15 +433,14 @@ def time_e2e(pkg, b: workloads.Batch, steps: int, dev) -> dict:
     conv, and copies the output planes back to pinned host memory.  Steps are
     pipelined over three streams and two device buffer sets: step i+1's
     upload and step i-1's download overlap step i's kernel."""
-    x_host = torch.from_numpy(np.ascontiguousarray(
-        b.x_buf[:, b.col_offset:b.col_offset + b.dim]).view(np.int16)).pin_memory()
+    x_host = torch.from_numpy(x_host_array(b, dense_x=True)).pin_memory()
     meta_host = [torch.from_numpy(a).pin_memory() for a in
                  (b.query_start_loc, b.cache_indices, b.has_initial_state)]
     bufs = [upload(b, dev, dense_x=True) for _ in range(2)]
     # one conv state shared by both sets: consecutive steps carry it along
     for s in bufs[1:]:
         s["conv_states"] = bufs[0]["conv_states"]
-    out_host = [torch.empty(bufs[0]["out"].shape, dtype=torch.int16).pin_memory()
+    out_host = [torch.empty(bufs[0]["out"].shape, dtype=out_dtype(b)).pin_memory()
                 for _ in range(2)]
     up, comp, down = (torch.cuda.Stream(device=dev) for _ in range(3))
     uploaded = [torch.cuda.Event() for _ in range(2)]
@@ -425,8 +477,9 @@ def time_e2e(pkg, b: workloads.Batch, steps: int, dev) -> dict:
     e1.record(down)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / steps
-    h2d = x_host.numel() * 2 + sum(h.numel() * h.element_size() for h in meta_host)
-    d2h = out_host[0].numel() * 2
+    h2d = x_host.numel() * x_host.element_size() + sum(h.numel() * h.element_size()
+                                                       for h in meta_host)
+    d2h = out_host[0].numel() * out_host[0].element_size()
     return {"ms": ms, "h2d": h2d, "d2h": d2h}
 
 
@@ -440,8 +493,9 @@ def oracle_sample(b: workloads.Batch, seconds: float, max_reps: int = 50) -> dic
     while reps < max_reps and (reps == 0 or t_total < seconds):
         st = b.conv_states.copy()
         t = time.perf_counter()
-        if st.dtype == np.uint16:  # bf16 state: the general-layout oracle
-            oracle.packed_conv1d_ex(b.x_buf, oracle.DTYPE_BF16, b.col_offset, b.dim, b.part_dim,
+        if st.dtype == np.uint16 or b.x_dtype != "bf16" or st.shape[2] != 3:  # general oracle
+            dt = {"bf16": oracle.DTYPE_BF16, "f16": oracle.DTYPE_F16, "f32": oracle.DTYPE_F32}
+            oracle.packed_conv1d_ex(b.x_buf, dt[b.x_dtype], b.col_offset, b.dim, b.part_dim,
                                     b.weight, b.bias, st, b.cache_indices, b.has_initial_state,
                                     b.query_start_loc, b.null_block_id, b.activation)
         else:
@@ -504,14 +558,27 @@ def base_line(args, world: int, value: float, ms: float, b: workloads.Batch, ext
             "workload": b.name, "tokens": b.tokens, "num_seqs": b.num_seqs, "dim": b.dim,
             "part_dim": b.part_dim, "x_row_stride": b.row_stride,
             "activation": "silu" if b.activation else "none", "bias": b.bias is not None,
-            "storage": ("x/out bf16, weight/bias fp32, conv_state "
-                        + ("bf16" if b.conv_states.dtype == np.uint16 else "fp32")),
+            "storage": (f"x/out {b.x_dtype}, weight/bias fp32, conv_state "
+                        + ("bf16" if b.conv_states.dtype == np.uint16 else "fp32")
+                        + f" width {b.conv_states.shape[2]}"),
+            "layout": dict(LAYOUT_OPTS),
             "bytes_per_step_per_gpu": workloads.algorithmic_bytes(b),
             "parallelism": f"replicas x{world}",
         },
     }
     line.update(extra)
     return line
+
+
+def make_workload(args) -> workloads.Batch:
+    """The named workload, stored as the --x-dtype / --state-width options say
+    (the same draws otherwise)."""
+    kw = {}
+    if args.x_dtype != "bf16":
+        kw["x_dtype"] = args.x_dtype
+    if args.state_width != 3:
+        kw["state_width"] = args.state_width
+    return workloads.WORKLOADS[args.workload](**kw)
 
 
 def run_reference(args) -> None:
@@ -522,7 +589,7 @@ def run_reference(args) -> None:
     from oracle import multicore
 
     oracle.load()
-    b = workloads.WORKLOADS[args.workload]()
+    b = make_workload(args)
     with multicore.OraclePool(b) as pool:  # the whole batch once, to size the sample
         pool.run(1)
         per_row = pool.run(1) / b.tokens
@@ -561,11 +628,11 @@ def run_ours(args) -> None:
     import linear_attention_prefill_varlen_gb300 as pkg
 
     pkg.lib()
-    b = workloads.WORKLOADS[args.workload]()
+    b = make_workload(args)
     if ENTRY == "update" and not (np.diff(b.query_start_loc) == 1).all():
         raise SystemExit("--entry update needs a batch of one-token sequences (e.g. --workload decode)")
     nbytes = workloads.algorithmic_bytes(b)
-    out_bytes = (b.dim // b.part_dim) * b.tokens * b.part_dim * 2
+    out_bytes = (b.dim // b.part_dim) * b.tokens * b.part_dim * (4 if b.x_dtype == "f32" else 2)
     footprint = b.x_buf.nbytes + out_bytes + b.conv_states.nbytes
     n_sets = min(max(3, -(-4 * L2_BYTES // footprint)), 16)
     sets = [upload(b, dev) for _ in range(n_sets)]
@@ -625,6 +692,8 @@ def run_ours(args) -> None:
                                 "the per-launch events); value from the launches' own time")
     line["config"]["kernel_source_sha"] = kernel_sha()
     line["config"]["entry"] = "kda_conv1d_update" if ENTRY == "update" else "kda_packed_conv1d"
+    if ENTRY != "update" and NORM is None and state_layout(pkg, b, upload_probe(b)) is not None:
+        line["config"]["entry"] = "kda_packed_conv1d_ex"
     if NORM is not None:
         line["config"]["entry"] += "_l2norm"
         line["config"]["qk_l2norm"] = {"planes": [0, 1], "head_dim": 128, "eps": 1e-6}
@@ -637,6 +706,14 @@ def main(argv=None) -> None:
     global ENTRY, NORM
     args = parse_args(argv)
     ENTRY = args.entry
+    LAYOUT_OPTS["state_layout"] = args.state_layout
+    LAYOUT_OPTS["weight_layout"] = args.weight_layout
+    global STORAGE_SUFFIX
+    STORAGE_SUFFIX = "".join([
+        f"_{args.x_dtype}" if args.x_dtype != "bf16" else "",
+        f"_k{args.state_width}" if args.state_width != 3 else "",
+        f"_state-{args.state_layout}" if args.state_layout != "dense" else "",
+        f"_weight-{args.weight_layout}" if args.weight_layout != "channel_major" else ""])
     if args.qk_l2norm and args.impl == "ours":
         import linear_attention_prefill_varlen_gb300 as pkg
 

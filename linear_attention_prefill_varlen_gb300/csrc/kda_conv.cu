@@ -102,6 +102,11 @@ struct Params {
     int64_t s_stride[3];  // element strides of conv_states: line, channel, position
     bool state_dense;     // K == 3 and strides (3 * dim, 3, 1)
     bool state_bf16;      // stored as bf16: read exactly, written rounded to nearest even
+    bool state_posvec;    // channels contiguous at each position (s_stride[1] == 1), line
+                          // and position strides multiples of 4, base aligned: the four
+                          // channels of a position move as one vector
+    bool weight_tapvec;   // tap-major weight (w_stride_c == 1, w_stride_j % 4 == 0,
+                          // 16-byte base): a tap's four channels are one float4
     const int32_t *cache_indices;
     const uint8_t *has_initial_state;
     const int32_t *qsl;
@@ -290,6 +295,36 @@ __device__ __forceinline__ void store_state3(void *sp, bool bf16, const float (&
                                 KDA_NS(4 * i + 3));
     }
 #undef KDA_NS
+}
+
+// Four consecutive conv-state elements starting at element i (i a multiple of
+// 4, the base aligned): one float4, or one 8-byte word of four bf16.
+__device__ __forceinline__ void state_get4(const Params &p, int64_t i, bool bf16,
+                                           float (&v)[4]) {
+    if (bf16) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(
+            static_cast<const uint16_t *>(p.conv_states) + i);
+        v[0] = __uint_as_float(u.x << 16);
+        v[1] = __uint_as_float(u.x & 0xFFFF0000u);
+        v[2] = __uint_as_float(u.y << 16);
+        v[3] = __uint_as_float(u.y & 0xFFFF0000u);
+    } else {
+        const float4 q = *reinterpret_cast<const float4 *>(static_cast<const float *>(p.conv_states) + i);
+        v[0] = q.x;
+        v[1] = q.y;
+        v[2] = q.z;
+        v[3] = q.w;
+    }
+}
+
+__device__ __forceinline__ void state_set4(const Params &p, int64_t i, bool bf16,
+                                           const float (&v)[4]) {
+    if (bf16)
+        *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(p.conv_states) + i) =
+            make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+    else
+        *reinterpret_cast<float4 *>(static_cast<float *>(p.conv_states) + i) =
+            make_float4(v[0], v[1], v[2], v[3]);
 }
 
 // Conv state element i (any layout), fp32 or bf16.
@@ -785,10 +820,12 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 
 // kLayout: 0 dense weight and dense fp32 state; 1 dense weight and dense bf16
 // state; 2 any strides, width and state type (kGeneral).
+// kLayout 3 (fp32 state) and 4 (bf16 state): the weight channel- or
+// tap-major and the state dense or position-major, every access a vector
+// (the flags weight_tapvec / state_posvec).
 template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
-__global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
+__global__ void __launch_bounds__(256, kLayout == 2 ? 2 : (kLayout == 3 ? 3 : 4))
     kda_conv1d_update_kernel(const Params p) {
-    constexpr bool kGeneral = kLayout == 2;
 #if KDA_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -802,7 +839,7 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     const int c = (int)(gid - token * nvec) * VEC;
 
     float w[VEC][4];
-    if (!kGeneral || p.weight_dense) {
+    if (kLayout < 2 || p.weight_dense) {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
             const float4 q = __ldg(reinterpret_cast<const float4 *>(p.weight) + (c + v));
@@ -810,6 +847,20 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
             w[v][1] = q.y;
             w[v][2] = q.z;
             w[v][3] = q.w;
+        }
+    } else if (kLayout >= 3) {
+        // tap-major: tap j of channels c .. c+3 is one float4
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int i = 0; i < VEC / 4; ++i) {
+                const float4 q = __ldg(reinterpret_cast<const float4 *>(
+                    p.weight + (int64_t)j * p.w_stride_j + c + 4 * i));
+                w[4 * i][j] = q.x;
+                w[4 * i + 1][j] = q.y;
+                w[4 * i + 2][j] = q.z;
+                w[4 * i + 3][j] = q.w;
+            }
         }
     } else {
 #pragma unroll
@@ -838,8 +889,8 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     const int64_t line = __ldg(p.cache_indices + token);
     const bool live = line != p.null_block_id;
     float h0[VEC], h1[VEC], h2[VEC];
-    if (!kGeneral || p.state_dense) {
-        const bool bf16 = kLayout == 1 || (kGeneral && p.state_bf16);
+    if (kLayout < 2 || p.state_dense) {
+        const bool bf16 = kLayout == 1 || kLayout == 4 || (kLayout == 2 && p.state_bf16);
         void *sp = state_line_ptr(p, line, c, bf16);
         float st[3 * VEC];
 #pragma unroll
@@ -861,6 +912,34 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
                 ns[2][v] = xv[v];
             }
             store_state3<VEC>(sp, bf16, ns);
+        }
+    } else if (kLayout >= 3) {
+        // Position-major: position k of channels c .. c+3 is one vector at
+        // base + k * s2.  Read positions K-3 .. K-1; then move positions
+        // 1 .. K-1 down by one (K-3 of them from registers) and write x at K-1.
+        static_assert(VEC == 4, "one vector per position");
+        constexpr bool bf16 = kLayout == 4;
+        const int K = p.state_width;
+        const int64_t s2 = p.s_stride[2];
+        const int64_t base = line * p.s_stride[0] + c;
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) h0[v] = h1[v] = h2[v] = 0.0f;
+        if (live) {
+            state_get4(p, base + (int64_t)(K - 3) * s2, bf16, h0);
+            state_get4(p, base + (int64_t)(K - 2) * s2, bf16, h1);
+            state_get4(p, base + (int64_t)(K - 1) * s2, bf16, h2);
+            // positions 0 .. K-5 take positions 1 .. K-4 in ascending order
+            // (each read before it is overwritten); none for K <= 4
+#pragma unroll 1
+            for (int k = 0; k + 4 < K; ++k) {
+                float v4[4];
+                state_get4(p, base + (int64_t)(k + 1) * s2, bf16, v4);
+                state_set4(p, base + (int64_t)k * s2, bf16, v4);
+            }
+            if (K > 3) state_set4(p, base + (int64_t)(K - 4) * s2, bf16, h0);
+            state_set4(p, base + (int64_t)(K - 3) * s2, bf16, h1);
+            state_set4(p, base + (int64_t)(K - 2) * s2, bf16, h2);
+            state_set4(p, base + (int64_t)(K - 1) * s2, bf16, xv);
         }
     } else {
         const int K = p.state_width;
@@ -953,6 +1032,18 @@ kda_status_t check_sizes(int64_t x_row_stride, int64_t tokens, int64_t dim, int6
 bool state_is_dense(const kda_conv_layout_t &l, int64_t dim) {
     return l.state_width == 3 && l.state_stride[0] == 3 * dim && l.state_stride[1] == 3 &&
            l.state_stride[2] == 1;
+}
+
+// Position-major state whose four-channel groups are aligned vectors.
+bool state_is_posvec(const kda_conv_layout_t &l, const void *conv_states) {
+    const uintptr_t vec_bytes = l.state_dtype == KDA_DTYPE_BF16 ? 8 : 16;
+    return l.state_stride[1] == 1 && l.state_stride[0] % 4 == 0 && l.state_stride[2] % 4 == 0 &&
+           aligned(conv_states, vec_bytes);
+}
+
+// Tap-major weight whose four-channel groups of a tap are aligned float4s.
+bool weight_is_tapvec(const kda_conv_layout_t &l, const float *weight) {
+    return l.weight_stride[0] == 1 && l.weight_stride[1] % 4 == 0 && aligned(weight, 16);
 }
 
 bool weight_is_dense(const kda_conv_layout_t &l) {
@@ -1193,6 +1284,8 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     for (int i = 0; i < 3; ++i) p.s_stride[i] = l.state_stride[i];
     p.state_dense = state_is_dense(l, dim);
     p.state_bf16 = l.state_dtype == KDA_DTYPE_BF16;
+    p.state_posvec = state_is_posvec(l, conv_states);
+    p.weight_tapvec = weight_is_tapvec(l, weight);
     p.cache_indices = cache_indices;
     p.has_initial_state = has_initial_state;
     p.qsl = query_start_loc;
@@ -1262,6 +1355,11 @@ void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s)
             dispatch_update_act<kDtype, 1>(p, blocks, silu, s);
         else
             dispatch_update_act<kDtype, 0>(p, blocks, silu, s);
+    else if ((p.weight_dense || p.weight_tapvec) && (p.state_dense || p.state_posvec))
+        if (p.state_bf16)
+            dispatch_update_act<kDtype, 4>(p, blocks, silu, s);
+        else
+            dispatch_update_act<kDtype, 3>(p, blocks, silu, s);
     else
         dispatch_update_act<kDtype, 2>(p, blocks, silu, s);
 }
@@ -1298,6 +1396,8 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     for (int i = 0; i < 3; ++i) p.s_stride[i] = l.state_stride[i];
     p.state_dense = state_is_dense(l, dim);
     p.state_bf16 = l.state_dtype == KDA_DTYPE_BF16;
+    p.state_posvec = state_is_posvec(l, conv_states);
+    p.weight_tapvec = weight_is_tapvec(l, weight);
     p.cache_indices = cache_indices;
     p.null_block_id = null_block_id;
     p.out = out;

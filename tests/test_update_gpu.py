@@ -244,3 +244,33 @@ def test_wrappers_prefill_then_decode_on_a_bf16_state():
         torch.cuda.synchronize()
         assert_states_equal(state_to_host(st), ref_st)
         _compare(d, o.view(torch.int16).cpu().numpy(), ref["out"])
+
+
+def test_update_position_major_state_at_an_unaligned_base():
+    """A position-major state whose base is 4 bytes off a 16-byte boundary
+    cannot move as vectors: the update must take the element path and still
+    match the oracle."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    b = _decode_batch(531, 64, 256, 128, 256, 100, null_count=2, state_width=4)
+    dev = torch.device("cuda")
+    pm = np.ascontiguousarray(b.conv_states.transpose(0, 2, 1))  # (lines, K, dim)
+    buf = torch.zeros(pm.size + 4, dtype=torch.float32, device=dev)
+    buf[1:1 + pm.size].copy_(torch.from_numpy(pm.ravel()))
+    st = buf[1:1 + pm.size].view(pm.shape).transpose(1, 2)  # (lines, dim, K) view
+    assert st.data_ptr() % 16 == 4
+    x = torch.from_numpy(b.x_buf.view(np.int16)).to(dev)
+    out = torch.full((b.dim // b.part_dim, b.tokens, b.part_dim), -1, dtype=torch.int16,
+                     device=dev)
+    w = torch.from_numpy(b.weight).to(dev)
+    bias = torch.from_numpy(b.bias).to(dev)
+    ci = torch.from_numpy(b.cache_indices).to(dev)
+    layout = pkg.make_layout(pkg.KDA_DTYPE_BF16, 4, st.stride(), w.stride())
+    pkg.kda_conv1d_update(x.data_ptr() + 2 * b.col_offset, b.row_stride, b.tokens, b.dim,
+                          b.part_dim, w, bias, st, ci, b.null_block_id, b.activation, out, layout)
+    torch.cuda.synchronize()
+    ref_st = b.conv_states.copy()
+    ref = pins.run_oracle_ex(b, states=ref_st)
+    assert_states_equal(st.contiguous().cpu().numpy(), ref_st)
+    _compare(b, out.cpu().numpy(), ref["out"])
+    assert buf[0].item() == 0.0 and buf[-3:].abs().sum().item() == 0.0  # guards untouched

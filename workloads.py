@@ -159,46 +159,49 @@ def _lengths(seed: int, n: int, lo: int, hi: int) -> list[int]:
     return torch.randint(lo, hi + 1, (n,), generator=g).tolist()
 
 
-def tiny() -> Batch:
+def tiny(**kw) -> Batch:
     # cache_indices = [2] as the workload fixes it, regardless of the permutation draw.
-    b = make_batch("tiny", 0, [64], 384, 128, 384, 4, his=[1])
+    b = make_batch("tiny", 0, [64], 384, 128, 384, 4, his=[1], **kw)
     b.cache_indices[:] = 2
     return b
 
 
-def varlen() -> Batch:
+# Each workload takes make_batch's x_dtype / state_width / state_dtype keywords
+# for the same draws stored another way (the general-layout measurements).
+
+def varlen(**kw) -> Batch:
     return make_batch("varlen", 1, _lengths(1, 8, 1, 512), 4608, 1536, 6400, 64,
-                      his_p=0.5, null_count=1)
+                      his_p=0.5, null_count=1, **kw)
 
 
-def long16k() -> Batch:
-    return make_batch("long16k", 2, [16384], 4608, 1536, 6400, 8, his=[1])
+def long16k(**kw) -> Batch:
+    return make_batch("long16k", 2, [16384], 4608, 1536, 6400, 8, his=[1], **kw)
 
 
-def short_decode() -> Batch:
+def short_decode(**kw) -> Batch:
     lens = _lengths(3, 256, 1, 128) + [1] * 1024
-    return make_batch("short_decode", 3, lens, 4608, 1536, 6400, 2048, his_p=0.8)
+    return make_batch("short_decode", 3, lens, 4608, 1536, 6400, 2048, his_p=0.8, **kw)
 
 
-def large_nobias() -> Batch:
+def large_nobias(**kw) -> Batch:
     return make_batch("large_nobias", 4, [8192] * 4, 3264, 1088, 3264, 16, x_std=2.0,
-                      w_range=1.0, bias_std=None, activation=0, his=[1, 0, 1, 0])
+                      w_range=1.0, bias_std=None, activation=0, his=[1, 0, 1, 0], **kw)
 
 
-def decode() -> Batch:
+def decode(**kw) -> Batch:
     """1024 sequences of one token each (a decode step), 2048 cache lines."""
-    return make_batch("decode", 5, [1] * 1024, 4608, 1536, 6400, 2048, his_p=1.0)
+    return make_batch("decode", 5, [1] * 1024, 4608, 1536, 6400, 2048, his_p=1.0, **kw)
 
 
-def decode_bf16_state() -> Batch:
+def decode_bf16_state(**kw) -> Batch:
     """The decode step with the conv state stored as bf16."""
     return make_batch("decode_bf16_state", 5, [1] * 1024, 4608, 1536, 6400, 2048, his_p=1.0,
-                      state_dtype="bf16")
+                      state_dtype="bf16", **kw)
 
 
-def spec_decode() -> Batch:
+def spec_decode(**kw) -> Batch:
     """1024 sequences of 4 tokens each, 2048 cache lines."""
-    return make_batch("spec_decode", 6, [4] * 1024, 4608, 1536, 6400, 2048, his_p=1.0)
+    return make_batch("spec_decode", 6, [4] * 1024, 4608, 1536, 6400, 2048, his_p=1.0, **kw)
 
 
 WORKLOADS = {
