@@ -175,7 +175,13 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
  * with a zero history and its line is not touched. The decode-step counterpart of
  * the conv update the kda_decode page's fused decode kernel performs. Layout as
  * for kda_packed_conv1d_ex (NULL: bf16 x, fp32 state, width 3, contiguous); with a
- * bf16 state the line is 6 bytes per channel instead of 12. Cache indices must
+ * bf16 state the line is 6 bytes per channel instead of 12. Besides the
+ * contiguous layout, two others move as vectors. One is a position-major state
+ * (channel stride 1, as a width-first (lines, K, dim) cache viewed as
+ * (lines, dim, K)) whose line and position strides are multiples of 4 and
+ * whose base is 16-byte (fp32) or 8-byte (bf16) aligned. The other is a
+ * tap-major weight (strides (1, a multiple of 4), 16-byte aligned). Other
+ * strides are read and written element by element. Cache indices must
  * be distinct (or null); out must not overlap x or conv_states. Asynchronous on
  * `stream`; allocates nothing.
  */
