@@ -984,7 +984,7 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : (kLayout == 3 ? 3 : 4)
     asm volatile("griddepcontrol.launch_dependents;" :::);
 #endif
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if constexpr (kLayout == 1) {
+    if constexpr (kLayout == 1 || kLayout == 4) {
         // The bf16-state step is short: a grid of 4 CTAs per SM looping over
         // the items beats one launch wave per 4 CTAs (measured on GB300:
         // 16.4 against 17.5 us for 1024 x 4608).  Lanes advance together, so
@@ -1377,7 +1377,9 @@ void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s)
             dispatch_update_act<kDtype, 0>(p, blocks, silu, s);
     else if ((p.weight_dense || p.weight_tapvec) && (p.state_dense || p.state_posvec))
         if (p.state_bf16)
-            dispatch_update_act<kDtype, 4>(p, blocks, silu, s);
+            dispatch_update_act<kDtype, 4>(
+                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
+                s);
         else
             dispatch_update_act<kDtype, 3>(p, blocks, silu, s);
     else
