@@ -984,11 +984,14 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : (kLayout == 3 ? 3 : 4)
     asm volatile("griddepcontrol.launch_dependents;" :::);
 #endif
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if constexpr (kLayout == 1 || kLayout == 4) {
-        // The bf16-state step is short: a grid of 4 CTAs per SM looping over
-        // the items beats one launch wave per 4 CTAs (measured on GB300:
-        // 16.4 against 17.5 us for 1024 x 4608).  Lanes advance together, so
-        // head groups stay whole for the L2 norm.
+    if constexpr (kLayout == 1 || kLayout >= 3) {
+        // A grid of (resident CTAs per SM) x SMs looping over the items: for
+        // the bf16-state and vector-layout steps it beats one thread per item
+        // (GB300, 1024 x 4608: bf16 dense 16.4 against 17.5 us, bf16
+        // position-major 18.9 against 20.1 us, fp32 position-major 28.4
+        // against 29.7 us); for the fp32 dense step it did not (23.3 against
+        // 23.0 us).  Lanes advance together, so head groups stay whole for
+        // the L2 norm.
         const int64_t total = (int64_t)p.tokens * (p.dim / VEC);
         const int64_t stride = (int64_t)gridDim.x * blockDim.x;
         for (int64_t g = gid; g < total; g += stride)
@@ -1381,7 +1384,9 @@ void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s)
                 p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
                 s);
         else
-            dispatch_update_act<kDtype, 3>(p, blocks, silu, s);
+            dispatch_update_act<kDtype, 3>(
+                p, blocks < 3 * (int64_t)current_sms() ? blocks : 3 * (int64_t)current_sms(), silu,
+                s);
     else
         dispatch_update_act<kDtype, 2>(p, blocks, silu, s);
 }
