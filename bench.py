@@ -130,7 +130,7 @@ class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
-             "clocks.mem,temperature.gpu")
+             "clocks.mem,temperature.gpu,temperature.memory")
 
     def __init__(self, device_index: int):
         self.device_index = device_index
@@ -169,7 +169,8 @@ class ClockSampler:
             if len(parts) < 9:
                 continue
             try:
-                extra = [float(p) for p in parts[9:11]] if len(parts) >= 11 else [None, None]
+                extra = [float(p) if p not in ("N/A", "[N/A]") else None for p in parts[9:12]]
+                extra += [None] * (3 - len(extra))
                 rows.append((float(parts[1]), float(parts[2]), parts[4:9], *extra))
             except ValueError:
                 continue
@@ -184,7 +185,10 @@ class ClockSampler:
                "reasons": reasons, "samples": len(rows)}
         if all(r[3] is not None for r in loaded):
             out["mem_mhz"] = statistics.median(r[3] for r in loaded)
+        if all(r[4] is not None for r in loaded):
             out["temp_c_max"] = max(r[4] for r in loaded)
+        if all(r[5] is not None for r in loaded):
+            out["mem_temp_c_max"] = max(r[5] for r in loaded)
         return out
 
 
