@@ -819,12 +819,13 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 // ---------------------------------------------------------------------------
 
 // kLayout: 0 dense weight and dense fp32 state; 1 dense weight and dense bf16
-// state; 2 any strides, width and state type (kGeneral).
-// kLayout 3 (fp32 state) and 4 (bf16 state): the weight channel- or
-// tap-major and the state dense or position-major, every access a vector
-// (the flags weight_tapvec / state_posvec).
+// state; 2 any strides, width and state type (the element path); 3 (fp32
+// state) and 4 (bf16 state): the weight channel- or tap-major and the state
+// dense or position-major, every access a vector (the flags weight_tapvec /
+// state_posvec).
+//
 // One (token, channel vector) of the decode update: the kernel below runs it
-// once per thread, or over a grid-stride loop (kLayout 1).
+// once per thread (kLayout 0, 2) or over a grid-stride loop (kLayout 1, 3, 4).
 template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
 __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
     constexpr int W = row_words<VEC, kDtype>();
@@ -977,7 +978,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
 }
 
 template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
-__global__ void __launch_bounds__(256, kLayout == 2 ? 2 : (kLayout == 3 ? 3 : 4))
+__global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     kda_conv1d_update_kernel(const Params p) {
 #if KDA_PDL
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -988,7 +989,7 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : (kLayout == 3 ? 3 : 4)
         // A grid of (resident CTAs per SM) x SMs looping over the items: for
         // the bf16-state and vector-layout steps it beats one thread per item
         // (GB300, 1024 x 4608: bf16 dense 16.4 against 17.5 us, bf16
-        // position-major 18.9 against 20.1 us, fp32 position-major 28.4
+        // position-major 18.9 against 20.1 us, fp32 position-major 26.5
         // against 29.7 us); for the fp32 dense step it did not (23.3 against
         // 23.0 us).  Lanes advance together, so head groups stay whole for
         // the L2 norm.
@@ -1385,7 +1386,7 @@ void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s)
                 s);
         else
             dispatch_update_act<kDtype, 3>(
-                p, blocks < 3 * (int64_t)current_sms() ? blocks : 3 * (int64_t)current_sms(), silu,
+                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
                 s);
     else
         dispatch_update_act<kDtype, 2>(p, blocks, silu, s);
