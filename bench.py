@@ -31,6 +31,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -135,7 +136,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.device_index = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{device_index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"kda_bench_clocks_gpu{device_index}.csv")
 
     def __enter__(self):
         try:
