@@ -448,6 +448,28 @@ def time_hot(pkg, b: workloads.Batch, sets: list, launches: int, dev) -> float:
     return e0.elapsed_time(e1) * 1e3 / launches
 
 
+def time_copy(nbytes: int, launches: int, dev) -> float:
+    """Context for the roofline: a plain device copy (torch copy_) moving the
+    same number of bytes as one launch (half read, half written), back to
+    back over rotating buffers larger than L2 in total.  Microseconds per
+    copy; outside the timed region."""
+    half = max(nbytes // 4, 1)  # int16 elements per side
+    n = max(2, -(-4 * L2_BYTES // (4 * half)))
+    bufs = [(torch.empty(half, dtype=torch.int16, device=dev),
+             torch.empty(half, dtype=torch.int16, device=dev)) for _ in range(n)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            bufs[i % n][1].copy_(bufs[i % n][0])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(launches):
+            bufs[i % n][1].copy_(bufs[i % n][0])
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) * 1e3 / launches
+
+
 def time_e2e(pkg, b: workloads.Batch, steps: int, dev) -> dict:
     """The same call with HOST inputs and result.  Every step copies its x
     (the (tokens, dim) slice) and metadata from pinned host memory, runs the
@@ -670,6 +692,7 @@ def run_ours(args) -> None:
         graph_us = dist.max(time_graph(pkg, b, sets, min(args.steps, 500), dev), dev)
     iso_min = dist.max(min(t["iso_ms"]), dev)
     hot_us = dist.max(time_hot(pkg, b, sets, min(max(args.steps, 1), 500), dev), dev)
+    copy_us = dist.max(time_copy(nbytes, min(max(args.steps, 1), 500), dev), dev)
 
     e2e = time_e2e(pkg, b, args.e2e_steps, dev)
     e2e_ms = dist.max(e2e["ms"], dev)
@@ -694,6 +717,10 @@ def run_ours(args) -> None:
                      "launch_us_isolated_min": round(iso_min * 1e3, 3),
                      "launch_us_graph_replay": None if graph_us is None else round(graph_us, 3),
                      "launch_us_hot_l2": round(hot_us, 3),
+                     "copy_us_same_bytes": round(copy_us, 3),
+                     "copy_same_bytes": ("torch copy_ of the launch's algorithmic bytes (half "
+                                         "read, half written), back to back over rotating "
+                                         "buffers; context for frac, not the value"),
                      "hot_l2": (f"one buffer set of {footprint / 1e6:.0f} MB every launch, back "
                                 f"to back ({'inside' if footprint <= L2_BYTES else 'larger than'}"
                                 f" the 129 MB L2); context only, not the value"),
