@@ -62,6 +62,9 @@
 #ifndef KDA_LOAD_L2_256
 #define KDA_LOAD_L2_256 0  // 1: x loads carry the L2::256B prefetch-size hint
 #endif
+#ifndef KDA_SHORT_PREFETCH
+#define KDA_SHORT_PREFETCH 6  // short-sequence kernel: rows beyond the queue fetched into L2 (0: off)
+#endif
 #ifndef KDA_STORE_CS
 #define KDA_STORE_CS 1  // 1: plane stores use the streaming (evict-first) cache hint
 #endif
@@ -513,6 +516,14 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
     return base;
 }
 
+// A hint to the TMA unit: bring `bytes` of global memory (16-byte aligned, a
+// multiple of 16 bytes) into L2.  It holds no register and nothing waits on it.
+__device__ __forceinline__ void l2_prefetch(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(__cvta_generic_to_global(ptr)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // The conv kernel
 // ---------------------------------------------------------------------------
@@ -535,6 +546,11 @@ __host__ __device__ constexpr int min_blocks() {
 // batches of short sequences: its mere presence costs the long-chunk path
 // about 3 % on GB300 (register allocation and scheduling of the main loop
 // shift), while it saves 10-15 % on batches of one- to five-token sequences.
+// Its steps also prefetch the rows KDA_SHORT_PREFETCH beyond the queue's
+// refill into L2 (16-bit x).  Such batches run many waves of warps, each exposing its
+// start-up latency, and the prefetch hides part of it (4.5 % on 256 short
+// prefills + 1024 decode tokens).  A single wave of long chunks already
+// saturates DRAM: there the same prefetch cost 8-12 %.
 // kNorm: planes in norm_mask get the per-head L2 norm after the activation.
 template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias,
           bool kShort, bool kNorm>
@@ -737,6 +753,15 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
                     store_out_row<VEC, kDtype>(static_cast<OT *>(p.out) + o + u * out_row, y[u]);
             }
         } else {
+            if constexpr (kShort && !kPreact && kDtype != KDA_DTYPE_F32 && KDA_SHORT_PREFETCH > 0) {
+                // Lane u < P: row t+P+D+u (D = KDA_SHORT_PREFETCH), the warp's
+                // whole row segment, while inside the chunk.
+                if (lane < P && t + (int64_t)(P + KDA_SHORT_PREFETCH) + lane < t1) {
+                    const int seg = min(32 * VEC, p.dim - (c - lane * VEC));
+                    l2_prefetch(xnext - lane * VEC + (int64_t)(KDA_SHORT_PREFETCH + lane) * xs,
+                                (uint32_t)(seg * (int)sizeof(XT)));
+                }
+            }
 #pragma unroll
             for (int u = 0; u < P; ++u) {
                 float xv[VEC];
