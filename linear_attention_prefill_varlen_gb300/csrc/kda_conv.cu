@@ -547,10 +547,10 @@ __host__ __device__ constexpr int min_blocks() {
 // about 3 % on GB300 (register allocation and scheduling of the main loop
 // shift), while it saves 10-15 % on batches of one- to five-token sequences.
 // Its steps also prefetch the rows KDA_SHORT_PREFETCH beyond the queue's
-// refill into L2 (16-bit x).  Such batches run many waves of warps, each exposing its
-// start-up latency, and the prefetch hides part of it (4.5 % on 256 short
-// prefills + 1024 decode tokens).  A single wave of long chunks already
-// saturates DRAM: there the same prefetch cost 8-12 %.
+// refill into L2 (16-bit x).  Such batches run many waves of warps, each
+// exposing its start-up latency, and the prefetch hides part of it (4.5 % on
+// 256 short prefills + 1024 decode tokens).  A single wave of long chunks
+// already saturates DRAM: there the same prefetch cost 8-12 %.
 // kNorm: planes in norm_mask get the per-head L2 norm after the activation.
 template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias,
           bool kShort, bool kNorm>
