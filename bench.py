@@ -454,7 +454,7 @@ def time_copy(nbytes: int, launches: int, dev) -> float:
     back over rotating buffers larger than L2 in total.  Microseconds per
     copy; outside the timed region."""
     half = max(nbytes // 4, 1)  # int16 elements per side
-    n = max(2, -(-4 * L2_BYTES // (4 * half)))
+    n = min(max(2, -(-4 * L2_BYTES // (4 * half))), launches + 20)  # no pair used twice in a row
     bufs = [(torch.empty(half, dtype=torch.int16, device=dev),
              torch.empty(half, dtype=torch.int16, device=dev)) for _ in range(n)]
     stream = torch.cuda.Stream(device=dev)
