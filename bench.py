@@ -380,7 +380,9 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
                 with torch.cuda.stream(stream):
                     flush.fill_(i & 0xFF)
                 starts[i].record(stream)
-            call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+            # the rotation continues from the warm-up: no step reuses the set
+            # of the step before it
+            call(pkg, b, sets[(warmup + i) % len(sets)], stream.cuda_stream)
             if flush is not None:
                 ends[i].record(stream)
         region1.record(stream)
@@ -400,7 +402,7 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
             with torch.cuda.stream(stream):
                 flush.fill_(i & 0xFF)
         s0.record(stream)
-        call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+        call(pkg, b, sets[(warmup + steps + i) % len(sets)], stream.cuda_stream)
         s1.record(stream)
     torch.cuda.synchronize(dev)
     iso_ms = [s0.elapsed_time(s1) for s0, s1 in iso]
