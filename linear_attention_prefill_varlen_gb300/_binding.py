@@ -219,11 +219,13 @@ def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: tor
     conv-state line cache_indices[i].  Returns (dim // part_dim, batch, part_dim)
     in x's dtype and shifts each touched line by one row, in place.
     `use_qk_l2norm` as for packed_causal_conv1d_fn."""
+    _check_conv_tensors(x, weight, bias, conv_states, out, part_dim, x.size(0) if x.dim() else 0)
     batch, dim = x.shape
+    _check_vector("cache_indices", cache_indices, batch, (torch.int32,))
+    _check_devices(x=x, weight=weight, bias=bias, conv_states=conv_states,
+                   cache_indices=cache_indices, out=out)
     if out is None:
         out = torch.empty((dim // part_dim, batch, part_dim), dtype=x.dtype, device=x.device)
-    if x.dtype not in _DTYPES:
-        raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
     act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
     norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
@@ -319,6 +321,49 @@ def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
     )
 
 
+def _check_vector(name: str, t: torch.Tensor, need: int, dtypes: tuple) -> None:
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} must be {' or '.join(str(d) for d in dtypes)}, not {t.dtype}")
+    if t.dim() != 1 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 1-D tensor")
+    if t.numel() < need:
+        raise ValueError(f"{name} has {t.numel()} entries, {need} needed")
+
+
+def _check_conv_tensors(x, weight, bias, conv_states, out, part_dim: int, rows: int) -> None:
+    """Dtypes and shapes the C ABI reads the wrappers' tensors with, checked
+    before any pointer reaches the library."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D (rows, dim) with unit channel stride")
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
+    dim = x.size(1)
+    if weight.dtype != torch.float32 or tuple(weight.shape) != (dim, 4):
+        raise ValueError(f"weight must be fp32 ({dim}, 4), not {weight.dtype} {tuple(weight.shape)}")
+    if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (dim,)
+                             or not bias.is_contiguous()):
+        raise ValueError(f"bias must be a contiguous fp32 ({dim},) tensor or None")
+    if (conv_states.dtype not in _STATE_DTYPES or conv_states.dim() != 3
+            or conv_states.size(1) != dim):
+        raise ValueError(f"conv_states must be fp32 or bf16 (lines, {dim}, width)")
+    if part_dim <= 0 or dim % part_dim != 0:
+        raise ValueError(f"part_dim {part_dim} must divide dim {dim}")
+    if out is not None:
+        shape = (dim // part_dim, rows, part_dim)
+        if out.dtype != x.dtype or tuple(out.shape) != shape or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous {x.dtype} {shape} tensor")
+
+
+def _check_devices(**tensors) -> None:
+    """Every tensor on x's CUDA device (there is no CPU path)."""
+    dev = tensors["x"].device
+    if dev.type != "cuda":
+        raise ValueError("x must be a CUDA tensor: the library has no CPU path")
+    for name, t in tensors.items():
+        if t is not None and t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, x on {dev}")
+
+
 def layout_of(x: torch.Tensor, weight: torch.Tensor, conv_states: torch.Tensor) -> KdaConvLayout:
     """The kda_conv_layout_t describing these tensors."""
     if conv_states.dtype not in _STATE_DTYPES:
@@ -342,19 +387,22 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
     library gets a value no cache index can hold).  `out` may be given to
     avoid the allocation.  `use_qk_l2norm` normalises each head_dim-channel
     head of planes 0 and 1 (q and k) per token, y / sqrt(sum y^2 + l2norm_eps)."""
+    _check_conv_tensors(x, weight, bias, conv_states, out, part_dim, x.size(0) if x.dim() else 0)
     tokens, dim = x.shape
-    num_seqs = query_start_loc.numel() - 1
+    num_seqs = max(query_start_loc.numel() - 1, 0)
+    _check_vector("query_start_loc", query_start_loc, 0, (torch.int32,))
+    _check_vector("cache_indices", cache_indices, num_seqs, (torch.int32,))
+    _check_vector("has_initial_state", has_initial_state, num_seqs, (torch.bool, torch.uint8))
+    _check_devices(x=x, weight=weight, bias=bias, conv_states=conv_states,
+                   query_start_loc=query_start_loc, cache_indices=cache_indices,
+                   has_initial_state=has_initial_state, out=out)
     if out is None:
         out = torch.empty((dim // part_dim, tokens, part_dim), dtype=x.dtype, device=x.device)
-    if has_initial_state.dtype != torch.uint8 and has_initial_state.dtype != torch.bool:
-        raise TypeError("has_initial_state must be bool or uint8")
-    if x.dtype not in _DTYPES:
-        raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
     act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
     norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
     kda_packed_conv1d_l2norm(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
                              cache_indices, has_initial_state, query_start_loc,
-                             max(num_seqs, 0), null, act, out, layout_of(x, weight, conv_states),
+                             num_seqs, null, act, out, layout_of(x, weight, conv_states),
                              norm, stream)
     return out
