@@ -51,7 +51,21 @@ MUTANTS = [
     # stays in bounds: bf16 stores into an fp32 state only touch the array's own bytes
     ("state_stored_as_bf16_always", "ref_store(conv_states, state_dtype,",
      "ref_store(conv_states, REF_DTYPE_BF16,"),
+    # the general-layout function's own copies of the basic steps
+    ("ex_his_ignored", "int read_state = (!is_null) && (has_initial_state[s] != 0);",
+     "int read_state = (!is_null);"),
+    ("ex_bias_dropped", "float acc = (bias != NULL) ? bias[c] : 0.0f;", "float acc = 0.0f;"),
+    ("ex_planes_row_major", "int64_t oi = (plane * tokens + (a + t)) * part_dim + col;",
+     "int64_t oi = (a + t) * dim + c;"),
+    ("ex_x_stride_ignored",
+     "float v = (r >= 0) ? ref_load(x, dtype, (a + r) * x_row_stride + c) : h[K + r];",
+     "float v = (r >= 0) ? ref_load(x, dtype, (a + r) * dim + c) : h[K + r];"),
+    # bf16 outputs and bf16 state rows truncated instead of rounded
+    ("bf16_store_truncates", "((uint16_t *)out)[i] = kda_ref_bf16_rne(y);",
+     "((uint16_t *)out)[i] = (uint16_t)(bits_from_f32(y) >> 16);"),
     # the q/k L2 norm
+    ("l2_first_head_only", "const float *v = y + r * width + h0;",
+     "const float *v = y + r * width;"),
     ("l2_eps_outside_root", "double d = sqrt(ss + eps);", "double d = sqrt(ss) + eps;"),
     ("l2_no_root", "double d = sqrt(ss + eps);", "double d = ss + eps;"),
     ("l2_abs_not_square", "ss += (double)v[i] * (double)v[i];", "ss += fabs((double)v[i]);"),
