@@ -777,8 +777,10 @@ def run_oracle_l2norm(b: workloads.Batch, norm_planes: int, head_dim: int, eps: 
 def pin_l2norm_conv(lib) -> None:
     """The conv with the norm folded in: planes outside the mask and the conv
     state are exactly the plain conv's; a normed plane's written rows have
-    heads of unit length up to bf16 rounding; unwritten rows stay untouched;
-    an empty mask is the plain conv."""
+    heads of unit length up to bf16 rounding, each pointing the way the same
+    head of the plain (activated) conv output points, so the norm follows the
+    activation; unwritten rows stay untouched; an empty mask is the plain
+    conv."""
     b = workloads.make_batch("l2conv", 181, [1, 2, 7, 40], 192, 64, 200, 7, col_offset=8,
                              his_p=0.6, null_count=1, tokens=55)
     st_plain, st_norm = b.conv_states.copy(), b.conv_states.copy()
@@ -793,6 +795,9 @@ def pin_l2norm_conv(lib) -> None:
         v = torch_bf16_to_f32(normed[plane][written]).astype(np.float64).reshape(-1, 2, 32)
         sq = (v * v).sum(axis=2)
         assert np.all(np.abs(sq - 1.0) < 2.0 ** -6), float(np.abs(sq - 1).max())
+        p = torch_bf16_to_f32(plain[plane][written]).astype(np.float64).reshape(-1, 2, 32)
+        unit = p / np.sqrt((p * p).sum(axis=2, keepdims=True))
+        assert np.all(np.abs(v - unit) < 2.0 ** -6), float(np.abs(v - unit).max())
     st3 = b.conv_states.copy()
     assert np.array_equal(run_oracle_l2norm(b, 0, 32, 1e-6, lib, states=st3)["out"], plain)
 

@@ -5,6 +5,7 @@ in a temporary directory), builds it and runs the pins against it: at least
 one pin has to fail.  The real oracle is never modified.
 """
 
+import inspect
 import os
 
 import pytest
@@ -92,6 +93,36 @@ def test_mutant_is_caught(name, old, new, tmp_path):
         try:
             pin(lib)
         except (AssertionError, ValueError) as e:  # ValueError: the mutant rejected a call
+            caught.append((pin.__name__, type(e).__name__))
+            break
+    assert caught, f"no pin caught mutant {name}"
+
+
+# The norm's composition (which planes, which rows, after the activation) is
+# Python in oracle/__init__.py; these mutants replace that function in the
+# module for one test, and the L2-norm pins must catch each.
+PY_MUTANTS = [
+    ("l2_mask_shifted", "if not (norm_planes >> plane) & 1:",
+     "if not (norm_planes >> (plane + 1)) & 1:"),
+    ("l2_before_activation", "normed = l2norm_heads(post[plane][rows]",
+     "normed = l2norm_heads(pre[plane][rows]"),
+    ("l2_every_row", "rows = ~np.isnan(pre[plane][:, 0])",
+     "rows = np.ones(pre.shape[1], dtype=bool)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_python_mutant_is_caught(name, old, new, monkeypatch, oracle_lib):
+    src = inspect.getsource(oracle.packed_conv1d_l2norm)
+    assert src.count(old) == 1, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), ns)
+    monkeypatch.setattr(oracle, "packed_conv1d_l2norm", ns["packed_conv1d_l2norm"])
+    caught = []
+    for pin in (pins.pin_l2norm_closed_forms, pins.pin_l2norm_invariants, pins.pin_l2norm_conv):
+        try:
+            pin(oracle_lib)
+        except (AssertionError, ValueError) as e:
             caught.append((pin.__name__, type(e).__name__))
             break
     assert caught, f"no pin caught mutant {name}"
