@@ -39,6 +39,24 @@ MUTANTS = [
      "int64_t o = (a + t) * dim + c;"),
     ("widen_shift", "return f32_from_bits((uint32_t)h << 16);",
      "return f32_from_bits(((uint32_t)h << 16) | 1u);"),
+    ("out_row_sequence_relative", "int64_t o = (plane * tokens + (a + t)) * part_dim + col;",
+     "int64_t o = (plane * tokens + t) * part_dim + col;"),
+    ("x_stride_is_dim",
+     "float v = (r >= 0) ? kda_ref_bf16_to_f32(x[(a + r) * x_row_stride + c])",
+     "float v = (r >= 0) ? kda_ref_bf16_to_f32(x[(a + r) * dim + c])"),
+    ("short_state_not_shifted",
+     "ns[k] = (r >= 0) ? kda_ref_bf16_to_f32(x[(a + r) * x_row_stride + c])\n"
+     "                                     : h[r + 3];",
+     "ns[k] = (r >= 0) ? kda_ref_bf16_to_f32(x[(a + r) * x_row_stride + c])\n"
+     "                                     : h[k];"),
+    ("empty_sequence_writes", "if (len <= 0) continue; /* an empty sequence",
+     "if (len < 0) continue; /* an empty sequence"),
+    ("silu_is_sigmoid", "return a / d;", "return 1.0f / d;"),
+    # the metadata check (the pins hand it bad metadata; the conv never gets any)
+    ("dup_not_detected", "for (int64_t r = 0; r < s; ++r) {", "for (int64_t r = 0; r < 0; ++r) {"),
+    ("qsl_end_unchecked", "if ((int64_t)query_start_loc[num_seqs] > tokens) {", "if (0) {"),
+    ("line_upper_unchecked", "if (line < 0 || line >= cache_lines) {", "if (line < 0) {"),
+    ("qsl_start_unchecked", "if (query_start_loc[0] < 0) {", "if (0) {"),
     # the general-layout function and the binary16 conversions
     ("ex_taps_first3", ": h[K + r];", ": h[3 + r];"),
     ("ex_state_not_shifted", ": h[k + len];", ": h[k];"),
