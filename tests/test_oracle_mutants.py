@@ -52,6 +52,7 @@ MUTANTS = [
     ("empty_sequence_writes", "if (len <= 0) continue; /* an empty sequence",
      "if (len < 0) continue; /* an empty sequence"),
     ("silu_is_sigmoid", "return a / d;", "return 1.0f / d;"),
+    ("bf16_nan_not_quieted", "return (uint16_t)(hi | 0x0040u);", "return (uint16_t)hi;"),
     # the metadata check (the pins hand it bad metadata; the conv never gets any)
     ("dup_not_detected", "for (int64_t r = 0; r < s; ++r) {", "for (int64_t r = 0; r < 0; ++r) {"),
     ("qsl_end_unchecked", "if ((int64_t)query_start_loc[num_seqs] > tokens) {", "if (0) {"),
@@ -64,6 +65,11 @@ MUTANTS = [
      "acc = fmaf(v, weight[c * 4 + j], acc);"),
     ("f16_ties_away", "if (rem > halfway || (rem == halfway && (kept & 1u))) kept += 1u;",
      "if (rem >= halfway) kept += 1u;"),
+    # 65504, the largest finite half, sent to infinity
+    ("f16_overflow_boundary", "if (a >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);",
+     "if (a >= 0x477FE000u) return (uint16_t)(sign | 0x7C00u);"),
+    ("f16_widen_no_specials",
+     "if (exp == 0x1Fu) return f32_from_bits(sign | 0x7F800000u | (frac << 13));", ""),
     ("f16_no_subnormals", "int q = (e >= -14) ? e - 10 : -24;", "int q = e - 10;"),
     ("f16_widen_subnormal", "float v = ldexpf((float)frac, -24);",
      "float v = ldexpf((float)frac, -25);"),
