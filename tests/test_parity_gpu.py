@@ -246,6 +246,26 @@ def test_many_sequences_four_search_levels():
     assert_outputs_match(d.out_bits(), ref["out"], b.activation)
 
 
+def test_short_batch_prefetch_on_a_half_warp_segment():
+    """A batch of short sequences (mean 14.3 rows: the short instantiation)
+    large enough for 24-row chunks, so its steps issue the L2 prefetch of
+    rows beyond the queue; dim 192, so each program's second warp covers 64
+    channels and prefetches 128-byte row segments.  x is a column slice of
+    a wider row (offset 8, stride 200)."""
+    rng = np.random.default_rng(702)
+    lengths = [1] * 2900 + [400] * 100
+    rng.shuffle(lengths)
+    b = workloads.make_batch("short_pf", 702, lengths, 192, 64, 200, 3010, col_offset=8,
+                             his_p=0.5, null_count=20)
+    assert b.tokens < 16 * b.num_seqs
+    ref, ref_states = oracle_run(b)
+    d = DeviceBatch(b)
+    d.run()
+    torch.cuda.synchronize()
+    assert_states_equal(d.states(), ref_states)
+    assert_outputs_match(d.out_bits(), ref["out"], b.activation)
+
+
 def test_offsets_beyond_32_bits():
     """40M token rows x 64 channels: the output plane offset and the x row
     offset of the last rows exceed 2^31 elements.  One 100-token sequence
