@@ -204,6 +204,13 @@ def spec_decode(**kw) -> Batch:
     return make_batch("spec_decode", 6, [4] * 1024, 4608, 1536, 6400, 2048, his_p=1.0, **kw)
 
 
+def skewed(**kw) -> Batch:
+    """One 8192-token prompt among 99 sequences of 80 tokens (16,112 tokens,
+    128 cache lines): many sequences, one of them long."""
+    lens = [80] * 50 + [8192] + [80] * 49
+    return make_batch("skewed", 7, lens, 4608, 1536, 6400, 128, his_p=0.8, **kw)
+
+
 WORKLOADS = {
     "tiny": tiny,
     "varlen": varlen,
@@ -213,6 +220,7 @@ WORKLOADS = {
     "decode": decode,
     "decode_bf16_state": decode_bf16_state,
     "spec_decode": spec_decode,
+    "skewed": skewed,
 }
 
 
