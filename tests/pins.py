@@ -805,3 +805,52 @@ def pin_l2norm_conv(lib) -> None:
 
 
 ALL_PINS += [pin_l2norm_closed_forms, pin_l2norm_invariants, pin_l2norm_conv]
+
+
+# --- the checker of the device epilogue over all 2^32 fp32 inputs ---
+
+FLT_MAX = float(np.finfo(np.float32).max)
+
+
+def ordered_bf16(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> integers that step by one per representable value."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    return np.where(b & 0x8000, 0x8000 - (b & 0x7FFF), 0x8000 + (b & 0x7FFF))
+
+
+def pin_silu_bf16_range(lib) -> None:
+    """kda_ref_silu_bf16_range, the host side of the exhaustive epilogue check
+    (the kda_conv page's module docstring, 3rd paragraph: SiLU, then rounding
+    to nearest even), over windows of 2^20 consecutive fp32 bit patterns:
+    denormals upwards from +0, around 1.0, across the expf overflow near
+    -88.72, up to +inf and into the NaNs, and one window that wraps from
+    0xFFFFFFFF (negative NaNs) to 0x00000000.
+
+    Element by element it is the rounding of the SiLU of the pattern at its
+    own index (the two parts are pinned on their own above).  Against torch's
+    float64 silu, rounded by torch to fp32 and then to bf16, it is within one
+    bf16 ulp with the same NaN class.  Where e^-a overflows fp32 (a below
+    -log(FLT_MAX)), the FP32 formula a / (1 + e^-a) is a / inf: -0."""
+    n = 1 << 20
+    thr = float(np.log(np.float64(FLT_MAX)))
+    for first in (0x00000000, 0x3F800000 - n // 2, 0xC2B17218 - n // 2, 0x7F800000 - n // 2,
+                  0xFFFFFFFF - n // 2 + 1):
+        got = oracle.silu_bf16_range(first, n, lib)
+        bits = ((np.arange(n, dtype=np.uint64) + np.uint64(first)) & np.uint64(0xFFFFFFFF))
+        a32 = bits.astype(np.uint32).view(np.float32)
+        assert np.array_equal(got, oracle.bf16_rne(oracle.silu(a32, lib), lib)), hex(first)
+        with np.errstate(invalid="ignore"):  # NaN patterns widen to NaN
+            a64 = a32.astype(np.float64)
+        ref32 = torch.nn.functional.silu(torch.from_numpy(a64)).to(torch.float32).numpy()
+        want = torch_f32_to_bf16(ref32)
+        nan_got, nan_want = is_nan_bf16(got), is_nan_bf16(want)
+        assert np.array_equal(nan_got, nan_want), hex(first)
+        with np.errstate(invalid="ignore"):
+            overflow = -a64 > thr * (1 + 1e-6)
+            regular = ~nan_want & ~(-a64 > thr * (1 - 1e-6))
+        assert (got[overflow] == 0x8000).all(), hex(first)
+        d = np.abs(ordered_bf16(got[regular]) - ordered_bf16(want[regular]))
+        assert d.size == 0 or d.max() <= 1, (hex(first), int(d.max()))
+
+
+ALL_PINS.append(pin_silu_bf16_range)

@@ -96,6 +96,13 @@ MUTANTS = [
     ("l2_abs_not_square", "ss += (double)v[i] * (double)v[i];", "ss += fabs((double)v[i]);"),
     ("l2_last_channel_dropped", "for (int64_t i = 0; i < head_dim; ++i) ss +=",
      "for (int64_t i = 0; i + 1 < head_dim; ++i) ss +="),
+    # the checker of the exhaustive epilogue test
+    ("range_index_off_by_one", "float a = f32_from_bits((uint32_t)(first + i));",
+     "float a = f32_from_bits((uint32_t)(first + i + 1));"),
+    ("range_not_rounded", "out[i] = kda_ref_bf16_rne(kda_ref_silu(a));",
+     "out[i] = (uint16_t)(bits_from_f32(kda_ref_silu(a)) >> 16);"),
+    ("range_no_silu", "out[i] = kda_ref_bf16_rne(kda_ref_silu(a));",
+     "out[i] = kda_ref_bf16_rne(a);"),
 ]
 
 
