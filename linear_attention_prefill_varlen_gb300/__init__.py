@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     KdaConvLayout,
     KdaError,
     KdaL2Norm,
+    activation_code,
     causal_conv1d_update,
     epilogue_range,
     kda_conv1d_update,

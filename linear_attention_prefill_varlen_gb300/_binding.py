@@ -219,6 +219,7 @@ def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: tor
     conv-state line cache_indices[i].  Returns (dim // part_dim, batch, part_dim)
     in x's dtype and shifts each touched line by one row, in place.
     `use_qk_l2norm` as for packed_causal_conv1d_fn."""
+    act = activation_code(activation)
     _check_conv_tensors(x, weight, bias, conv_states, out, part_dim, x.size(0) if x.dim() else 0)
     batch, dim = x.shape
     _check_vector("cache_indices", cache_indices, batch, (torch.int32,))
@@ -226,7 +227,6 @@ def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: tor
                    cache_indices=cache_indices, out=out)
     if out is None:
         out = torch.empty((dim // part_dim, batch, part_dim), dtype=x.dtype, device=x.device)
-    act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
     norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
     kda_conv1d_update_l2norm(x, x.stride(0), batch, dim, part_dim, weight, bias, conv_states,
@@ -295,7 +295,22 @@ def epilogue_range(first: int, count: int, activation: int, out, stream=None) ->
     _check(lib().kda_epilogue_range(first, count, activation, _ptr(out), _stream(stream)))
 
 
-_SILU_NAMES = ("silu", "swish", True)
+_SILU_NAMES = ("silu", "swish")
+_NONE_NAMES = ("none", "identity")
+
+
+def activation_code(activation) -> int:
+    """The kda_activation_t of a wrapper's `activation`: "silu", "swish" or
+    True select SiLU; None, False, "none" or "identity" select none.  Any
+    other value (another name, a different case, an integer) is a ValueError
+    rather than a silent choice."""
+    if activation is True or (isinstance(activation, str) and activation in _SILU_NAMES):
+        return KDA_ACT_SILU
+    if activation is None or activation is False or (
+            isinstance(activation, str) and activation in _NONE_NAMES):
+        return KDA_ACT_NONE
+    raise ValueError(f"activation must be 'silu', 'swish', True, None, False, 'none' or "
+                     f"'identity', not {activation!r}")
 _DTYPES = {torch.bfloat16: KDA_DTYPE_BF16, torch.float16: KDA_DTYPE_F16,
            torch.float32: KDA_DTYPE_F32}
 _STATE_DTYPES = {torch.float32: KDA_DTYPE_F32, torch.bfloat16: KDA_DTYPE_BF16}
@@ -382,11 +397,12 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
     """Varlen causal depthwise conv of x (tokens, dim), dim = parts x part_dim.
 
     Returns (dim // part_dim, tokens, part_dim) in x's dtype; conv_states is
-    updated in place.  `activation` in ("silu", "swish", True) selects SiLU,
-    anything else none.  `null_block_id=None` disables padding detection (the
+    updated in place.  `activation` "silu", "swish" or True selects SiLU;
+    None, False, "none" or "identity" none; anything else is a ValueError.  `null_block_id=None` disables padding detection (the
     library gets a value no cache index can hold).  `out` may be given to
     avoid the allocation.  `use_qk_l2norm` normalises each head_dim-channel
     head of planes 0 and 1 (q and k) per token, y / sqrt(sum y^2 + l2norm_eps)."""
+    act = activation_code(activation)
     _check_conv_tensors(x, weight, bias, conv_states, out, part_dim, x.size(0) if x.dim() else 0)
     tokens, dim = x.shape
     num_seqs = max(query_start_loc.numel() - 1, 0)
@@ -398,7 +414,6 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
                    has_initial_state=has_initial_state, out=out)
     if out is None:
         out = torch.empty((dim // part_dim, tokens, part_dim), dtype=x.dtype, device=x.device)
-    act = KDA_ACT_SILU if activation in _SILU_NAMES else KDA_ACT_NONE
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
     norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
     kda_packed_conv1d_l2norm(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,

@@ -74,3 +74,28 @@ def test_update_wrapper_rejects(ci, exc, words):
     with pytest.raises(exc, match=words):
         pkg.causal_conv1d_update(x, torch.zeros(LINES, DIM, 3), torch.zeros(DIM, 4),
                                  torch.zeros(DIM), ci, PART)
+
+
+@pytest.mark.parametrize("value,code", [
+    ("silu", pkg.KDA_ACT_SILU), ("swish", pkg.KDA_ACT_SILU), (True, pkg.KDA_ACT_SILU),
+    (None, pkg.KDA_ACT_NONE), (False, pkg.KDA_ACT_NONE), ("none", pkg.KDA_ACT_NONE),
+    ("identity", pkg.KDA_ACT_NONE),
+])
+def test_activation_values_accepted(value, code):
+    assert pkg.activation_code(value) == code
+
+
+@pytest.mark.parametrize("value", ["SiLU", "gelu", "relu", "", 1, 0, 1.0, "Silu "])
+def test_activation_values_rejected(value):
+    with pytest.raises(ValueError, match="activation"):
+        pkg.activation_code(value)
+    a = _prefill()
+    with pytest.raises(ValueError, match="activation"):  # before any other check
+        pkg.packed_causal_conv1d_fn(a["x"], a["weight"], a["bias"], a["conv_states"],
+                                    a["query_start_loc"], a["cache_indices"],
+                                    a["has_initial_state"], PART, activation=value)
+    with pytest.raises(ValueError, match="activation"):
+        pkg.causal_conv1d_update(torch.zeros(4, DIM, dtype=torch.bfloat16),
+                                 torch.zeros(LINES, DIM, 3), torch.zeros(DIM, 4),
+                                 torch.zeros(DIM), torch.zeros(4, dtype=torch.int32), PART,
+                                 activation=value)
