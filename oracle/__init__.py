@@ -74,7 +74,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         getattr(lib, name).restype = None
     lib.kda_ref_packed_conv1d_ex.argtypes = [
         P, ctypes.c_int, I64, I64, I64, I64,  # x, dtype, x_row_stride, tokens, dim, part_dim
-        P, I64, I64, P,  # weight, w_stride_c, w_stride_j, bias
+        P, I64, I64, I64, P,  # weight, w_stride_c, w_stride_j, w_stride_part, bias
         P, ctypes.c_int, I64, I64, I64, I64, I64,  # conv_states, state dtype, lines, width, strides
         P, P, P, I64, I64,  # cache_indices, has_initial_state, qsl, num_seqs, null_block_id
         ctypes.c_int, P, P,  # activation, out, preact
@@ -236,7 +236,9 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
 
     ``x_buf`` (tokens, row_stride): uint16 bits for bf16 / fp16, float32 for
     fp32; the input is columns [col_offset, col_offset + dim).  ``weight`` is
-    a (dim, 4) float32 view with any strides; ``conv_states`` a
+    a (dim, 4) float32 view with any strides, or a (dim / part_dim, 4,
+    part_dim) view (part, tap, channel within the part: the width-major
+    decode weight of the kda_decode page) with any strides; ``conv_states`` a
     (lines, dim, K) view with any strides, float32 or uint16 (bf16 bits),
     updated in place.  Returns
     ``out`` (dim/part_dim, tokens, part_dim) of x's storage type, filled with
@@ -246,11 +248,18 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
     assert x_buf.ndim == 2 and x_buf.flags["C_CONTIGUOUS"]
     assert (x_buf.dtype == np.float32) == (dtype == DTYPE_F32)
     tokens, row_stride = x_buf.shape
-    assert weight.dtype == np.float32 and weight.shape == (dim, 4)
+    assert weight.dtype == np.float32
+    if weight.ndim == 2:
+        assert weight.shape == (dim, 4)
+        ws = _elem_strides(weight)
+        w_c, w_j, w_part = ws[0], ws[1], part_dim * ws[0]
+    else:
+        assert weight.shape == (dim // part_dim, 4, part_dim)
+        ws = _elem_strides(weight)
+        w_c, w_j, w_part = ws[2], ws[1], ws[0]
     assert conv_states.dtype in (np.float32, np.uint16) and conv_states.ndim == 3
     state_dtype = DTYPE_F32 if conv_states.dtype == np.float32 else DTYPE_BF16
     assert conv_states.shape[1] == dim
-    ws = _elem_strides(weight)
     ss = _elem_strides(conv_states)
     bias = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
     ci = np.ascontiguousarray(cache_indices, dtype=np.int32)
@@ -264,7 +273,7 @@ def packed_conv1d_ex(x_buf: np.ndarray, dtype: int, col_offset: int, dim: int, p
     preact = np.full(out.shape, np.nan, dtype=np.float32) if want_preact else None
     rc = lib.kda_ref_packed_conv1d_ex(
         x_buf.ctypes.data + x_buf.itemsize * col_offset, dtype, row_stride, tokens, dim, part_dim,
-        weight.ctypes.data, ws[0], ws[1], _ptr(bias),
+        weight.ctypes.data, w_c, w_j, w_part, _ptr(bias),
         conv_states.ctypes.data, state_dtype, conv_states.shape[0], conv_states.shape[2],
         ss[0], ss[1], ss[2],
         _ptr(ci), _ptr(his), _ptr(qsl), qsl.size - 1, null_block_id, activation,

@@ -307,7 +307,13 @@ static void ref_store(void *out, int dtype, int64_t i, float y) {
  *   x and out are of type `dtype` (bf16, fp16 or fp32; out has x's type, as
  *   packed_causal_conv1d_fn returns x.dtype); fp16 / bf16 outputs are rounded
  *   to nearest even, fp32 outputs are the FP32 result itself;
- *   weight[c][j] is at weight[c * w_stride_c + j * w_stride_j];
+ *   weight[c][j] is at weight[(c / part_dim) * w_stride_part +
+ *   (c % part_dim) * w_stride_c + j * w_stride_j]: a (dim, 4) weight with
+ *   strides (s_c, s_j) is w_stride_part = part_dim * s_c; the width-major
+ *   decode weight of "vllm.models.kimi_k3.amd.ops.kda_decode"
+ *   (make_decode_conv1d_weight_loader: indexed [qkv, width, channel], the
+ *   channel contiguous) is a (dim / part_dim, 4, part_dim) buffer with
+ *   w_stride_part = 4 * part_dim, w_stride_j = part_dim, w_stride_c = 1;
  *   the conv state of a line holds the K = state_width most recent rows,
  *   position K-1 the newest, element (line, c, k) at
  *   conv_states[line * s_stride_line + c * s_stride_c + k * s_stride_k].
@@ -319,7 +325,8 @@ static void ref_store(void *out, int dtype, int64_t i, float y) {
  */
 int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int64_t tokens,
                              int64_t dim, int64_t part_dim, const float *weight,
-                             int64_t w_stride_c, int64_t w_stride_j, const float *bias,
+                             int64_t w_stride_c, int64_t w_stride_j, int64_t w_stride_part,
+                             const float *bias,
                              void *conv_states, int state_dtype, int64_t cache_lines,
                              int64_t state_width,
                              int64_t s_stride_line, int64_t s_stride_c, int64_t s_stride_k,
@@ -356,13 +363,14 @@ int kda_ref_packed_conv1d_ex(const void *x, int dtype, int64_t x_row_stride, int
                                   : 0.0f;
             int64_t plane = c / part_dim;
             int64_t col = c % part_dim;
+            int64_t wbase = plane * w_stride_part + col * w_stride_c;
 
             for (int64_t t = 0; t < len; ++t) {
                 float acc = (bias != NULL) ? bias[c] : 0.0f;
                 for (int j = 0; j <= 3; ++j) {
                     int64_t r = t - 3 + j;
                     float v = (r >= 0) ? ref_load(x, dtype, (a + r) * x_row_stride + c) : h[K + r];
-                    acc = fmaf(v, weight[c * w_stride_c + j * w_stride_j], acc);
+                    acc = fmaf(v, weight[wbase + j * w_stride_j], acc);
                 }
                 float y = activation ? kda_ref_silu(acc) : acc;
                 int64_t oi = (plane * tokens + (a + t)) * part_dim + col;

@@ -676,7 +676,9 @@ def pin_ex_state_width(lib) -> None:
 
 def pin_ex_strides(lib) -> None:
     """The same call with the state stored position-major and the weight
-    tap-major (width-major) gives the same outputs and the same state values."""
+    tap-major (width-major), or the weight as the kda_decode page's
+    [qkv, width, channel] buffer (packed or padded), gives the same outputs
+    and the same state values."""
     K = 4
     b = workloads.make_batch("strides", 151, [3, 12, 1], 128, 64, 136, 6, col_offset=8,
                              his_p=0.7, null_count=1, state_width=K)
@@ -688,6 +690,21 @@ def pin_ex_strides(lib) -> None:
     got = run_oracle_ex(b, lib, weight=mem_w.T, states=view_s)
     assert np.array_equal(got["out"], ref["out"])
     assert np.array_equal(np.ascontiguousarray(view_s).view(np.uint32), st.view(np.uint32))
+    # The kda_decode page's width-major decode weight, [qkv, width, channel]
+    # with the channel contiguous (make_decode_conv1d_weight_loader): part i,
+    # tap j, channel q of the part is weight[i * part_dim + q][j].
+    parts = b.dim // b.part_dim
+    w3 = np.ascontiguousarray(b.weight.reshape(parts, b.part_dim, 4).transpose(0, 2, 1))
+    st3 = b.conv_states.copy()
+    got3 = run_oracle_ex(b, lib, weight=w3, states=st3)
+    assert np.array_equal(got3["out"], ref["out"])
+    assert np.array_equal(st3.view(np.uint32), st.view(np.uint32))
+    # the same buffer with padding between parts and between taps
+    pad = np.zeros((parts, 5, b.part_dim + 8), dtype=np.float32)
+    pad[:, :4, 4:4 + b.part_dim] = w3
+    st4 = b.conv_states.copy()
+    got4 = run_oracle_ex(b, lib, weight=pad[:, :4, 4:4 + b.part_dim], states=st4)
+    assert np.array_equal(got4["out"], ref["out"])
 
 
 ALL_PINS += [pin_f16_widen, pin_f16_rne, pin_ex_matches_basic, pin_ex_typed_exact,

@@ -61,8 +61,13 @@ MUTANTS = [
     # the general-layout function and the binary16 conversions
     ("ex_taps_first3", ": h[K + r];", ": h[3 + r];"),
     ("ex_state_not_shifted", ": h[k + len];", ": h[k];"),
-    ("ex_weight_stride_ignored", "acc = fmaf(v, weight[c * w_stride_c + j * w_stride_j], acc);",
+    ("ex_weight_stride_ignored", "acc = fmaf(v, weight[wbase + j * w_stride_j], acc);",
      "acc = fmaf(v, weight[c * 4 + j], acc);"),
+    ("ex_weight_part_stride_ignored",
+     "int64_t wbase = plane * w_stride_part + col * w_stride_c;",
+     "int64_t wbase = c * w_stride_c;"),
+    ("ex_weight_part_index_off", "int64_t wbase = plane * w_stride_part + col * w_stride_c;",
+     "int64_t wbase = (dim / part_dim - 1 - plane) * w_stride_part + col * w_stride_c;"),
     ("f16_ties_away", "if (rem > halfway || (rem == halfway && (kept & 1u))) kept += 1u;",
      "if (rem >= halfway) kept += 1u;"),
     # 65504, the largest finite half, sent to infinity
