@@ -110,19 +110,31 @@ def profile_path(entry: str, workload: str) -> str:
     return os.path.join(PROFILES, f"{kernel}_{workload}{STORAGE_SUFFIX}.md")
 
 
-def recorded_traffic(entry: str, workload: str) -> int | None:
-    """Per-launch DRAM bytes from the committed ncu summary of this kernel on
-    this workload, if there is one and it was taken on the current kernel
-    source (its sha line matches)."""
+def recorded_traffic(entry: str, workload: str) -> dict:
+    """Per-launch DRAM bytes (read + write, and each side) recorded from one
+    ncu capture in the committed summary of this kernel on this workload, if
+    there is one and it was taken on the current kernel source (its sha line
+    matches); otherwise None for each."""
+    none = {"traffic": None, "traffic_read": None, "traffic_write": None,
+            "traffic_source": None}
     try:
-        text = open(profile_path(entry, workload)).read()
+        path = profile_path(entry, workload)
+        text = open(path).read()
     except OSError:
-        return None
+        return none
     sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
     tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    rd = re.search(r"dram_read_bytes_per_launch:\s*([0-9]+)", text)
+    wr = re.search(r"dram_write_bytes_per_launch:\s*([0-9]+)", text)
     if not sha or not tr or sha.group(1) != kernel_sha():
-        return None
-    return int(tr.group(1))
+        return none
+    return {"traffic": int(tr.group(1)),
+            "traffic_read": int(rd.group(1)) if rd else None,
+            "traffic_write": int(wr.group(1)) if wr else None,
+            "traffic_source": ("recorded: dram__bytes_read.sum / dram__bytes_write.sum of one "
+                               "ncu launch (caches flushed before it; writes still dirty in L2 "
+                               "when it ends are not counted), "
+                               + os.path.relpath(path, ROOT))}
 
 
 class ClockSampler:
@@ -146,9 +158,20 @@ class ClockSampler:
                 ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        # nvidia-smi's start-up (NVML initialisation) slows kernel launches
+        # down while it runs: wait for its first sample before going on.
+        t_end = time.perf_counter() + 10.0
+        while time.perf_counter() < t_end and self.proc.poll() is None:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    break
+            except OSError:
+                pass
+            time.sleep(0.02)
+        time.sleep(0.1)
         return self
 
     def __exit__(self, *exc):
@@ -348,10 +371,31 @@ def call(pkg, b: workloads.Batch, s: dict, stream) -> None:
                           b.null_block_id, b.activation, s["out"], stream)
 
 
+SETTLE_S = 0.2
+
+
+def settle(dev, stream, seconds: float = SETTLE_S) -> None:
+    """Device copies between two 256 MB scratch buffers for about `seconds`,
+    ending right before the warm-up steps, so that the GPU's clocks and power
+    state are those of a busy GPU (as between a model's layers) when the
+    warm-up and the timed region start.  Outside the timed region; the
+    buffers are freed afterwards."""
+    a = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    c = torch.empty_like(a)
+    t_end = time.perf_counter() + seconds
+    with torch.cuda.stream(stream):
+        while time.perf_counter() < t_end:
+            for _ in range(16):
+                c.copy_(a)
+            stream.synchronize()
+    del a, c
+
+
 def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, dist: Dist,
                 dev, flush: torch.Tensor | None = None) -> dict:
     """W untimed steps, then exactly K timed steps between barrier+sync pairs,
-    each step on the next input/output set, on one stream.
+    each step on the next input/output set, on one stream.  Before the
+    warm-up, `settle` keeps the GPU busy for 0.2 s with device copies.
 
     Without `flush` the K launches run back to back between two region events
     (as a model's layers would issue them); the average launch duration is the
@@ -361,9 +405,6 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
     outside the timed region, up to 200 more launches with per-launch events
     give the isolated launch time."""
     stream = torch.cuda.Stream(device=dev)
-    for i in range(warmup):
-        call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
-    torch.cuda.synchronize(dev)
 
     def ev():
         return torch.cuda.Event(enable_timing=True)
@@ -371,9 +412,15 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
     starts = [ev() for _ in range(steps)] if flush is not None else []
     ends = [ev() for _ in range(steps)] if flush is not None else []
     region0, region1 = ev(), ev()
-    dist.barrier()
-    torch.cuda.synchronize(dev)
+    # The clock sampler starts before the warm-up, and the GPU is kept busy
+    # from there to the timed region: an idle GPU, or nvidia-smi still
+    # starting, slowed a 20-step region down by 2-9 % on GB300.
     with ClockSampler(dev.index or 0) as clocks:
+        settle(dev, stream)
+        for i in range(warmup):
+            call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+        dist.barrier()
+        torch.cuda.synchronize(dev)
         region0.record(stream)
         for i in range(steps):
             if flush is not None:
@@ -711,7 +758,7 @@ def run_ours(args) -> None:
                         else None),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(ENTRY, b.name), "peak_source": peak_kind,
+                     **recorded_traffic(ENTRY, b.name), "peak_source": peak_kind,
                      "kernel": ("kda_conv1d_update_kernel" if ENTRY == "update"
                                 else "kda_packed_conv1d_kernel"),
                      "launch_us_mean": round(ms_per_step * 1e3, 3),
@@ -745,6 +792,9 @@ def run_ours(args) -> None:
     else:
         line["config"]["l2"] = ("a 512 MB buffer rewritten before every step (L2 flush, outside "
                                 "the per-launch events); value from the launches' own time")
+    line["config"]["settle"] = (f"{SETTLE_S} s of device copies right before the warm-up "
+                                f"steps (clocks and power state of a busy GPU); outside the "
+                                f"timed region")
     line["config"]["kernel_source_sha"] = kernel_sha()
     line["config"]["entry"] = "kda_conv1d_update" if ENTRY == "update" else "kda_packed_conv1d"
     if ENTRY != "update" and NORM is None and state_layout(pkg, b, upload_probe(b)) is not None:
