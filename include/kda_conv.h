@@ -94,7 +94,24 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F16 = 1, KDA_DTYPE_F32 = 2 } kda_dt
  *                  kda_conv page keeps the state in FP32; the kda_decode page's
  *                  fused decode kernel (is_fused_kda_decode_supported) takes a
  *                  bf16 conv state only. bf16 halves a decode step's state traffic.
- *   reserved       must be 0.
+ *   version        0 or 1 (any other value is KDA_ERR_INVALID_ARG). With 0 the
+ *                  struct ends here: the library reads none of the fields below,
+ *                  so a caller may pass the shorter struct of earlier releases.
+ *                  With 1 the two fields below are read as well.
+ *   weight_part_stride   (version 1) element stride between the parts of the
+ *                  weight, for a weight that is not one (dim, 4) array: weight[c][j]
+ *                  is at (c / part_dim) * weight_part_stride + (c % part_dim) *
+ *                  weight_stride[0] + j * weight_stride[1]. 0 means part_dim *
+ *                  weight_stride[0], i.e. the (dim, 4) form above. The width-major
+ *                  decode weight of the vLLM page "vllm.models.kimi_k3.amd.ops.
+ *                  kda_decode" (make_decode_conv1d_weight_loader: indexed
+ *                  [qkv, width, channel], the channel contiguous) is a
+ *                  (dim / part_dim, 4, part_dim) buffer: weight_stride = (1,
+ *                  part_dim), weight_part_stride = 4 * part_dim.
+ *   cache_index_stride   (version 1) elements between consecutive cache_indices
+ *                  entries (sequence s uses cache_indices[s * stride]), as the
+ *                  kda_conv page's packed_causal_conv1d_fn passes
+ *                  cache_indices.stride(0) to its kernel; 0 means 1. Must be >= 0.
  */
 typedef struct kda_conv_layout {
     int32_t x_dtype;
@@ -102,7 +119,9 @@ typedef struct kda_conv_layout {
     int64_t state_stride[3];
     int64_t weight_stride[2];
     int32_t state_dtype;
-    int32_t reserved;
+    int32_t version;
+    int64_t weight_part_stride; /* read only when version >= 1 */
+    int64_t cache_index_stride; /* read only when version >= 1 */
 } kda_conv_layout_t;
 
 /*
@@ -152,7 +171,8 @@ kda_status_t kda_packed_conv1d(const void *x, int64_t x_row_stride, int64_t toke
  * state_dtype. Rounding of out: bf16 and fp16 to nearest even, fp32 none.
  * Alignment: x and out 16-byte aligned and x_row_stride a multiple of 16 bytes
  * (8 elements of bf16 / fp16, 4 of fp32); weight 16-byte aligned when its strides
- * are (4, 1), else 4-byte; conv_states 16-byte aligned when it is width 3 and
+ * are (4, 1) (and the part stride 4 * part_dim), else 4-byte; conv_states
+ * 16-byte aligned when it is width 3 and
  * contiguous, else aligned to its element; bias 16-byte aligned. Everything else
  * as for kda_packed_conv1d.
  */
@@ -208,7 +228,10 @@ kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batc
  *   plane_mask  bit i: normalise output plane i (Q|K|V packing: 0x3 for q, k).
  *               0 = no norm. Bits at or above dim / part_dim are an error.
  *   head_dim    channels per head: 4, 8, 16, 32, 64 or 128, dividing part_dim.
- *   eps         >= 0, finite. With eps = 0 an all-zero head gives NaN.
+ *   eps         0, or a normal finite number (>= FLT_MIN, about 1.18e-38); a
+ *               subnormal eps is KDA_ERR_INVALID_ARG, because the reciprocal root
+ *               flushes subnormal inputs to zero. With eps = 0 a head whose sum of
+ *               squares is zero or subnormal comes out NaN or inf.
  *   reserved    must be 0.
  */
 typedef struct kda_l2norm {

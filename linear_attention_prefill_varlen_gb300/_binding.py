@@ -35,18 +35,24 @@ class KdaError(RuntimeError):
 
 
 class KdaConvLayout(ctypes.Structure):
-    """kda_conv_layout_t: x/out dtype, conv-state width, element strides and
-    conv-state dtype."""
+    """kda_conv_layout_t (version 1): x/out dtype, conv-state width, element
+    strides, conv-state dtype, the weight's part stride and the stride of
+    cache_indices."""
 
     _fields_ = [("x_dtype", ctypes.c_int32), ("state_width", ctypes.c_int32),
                 ("state_stride", ctypes.c_int64 * 3), ("weight_stride", ctypes.c_int64 * 2),
-                ("state_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("state_dtype", ctypes.c_int32), ("version", ctypes.c_int32),
+                ("weight_part_stride", ctypes.c_int64), ("cache_index_stride", ctypes.c_int64)]
 
 
 def make_layout(x_dtype: int, state_width: int, state_stride, weight_stride,
-                state_dtype: int = KDA_DTYPE_F32) -> KdaConvLayout:
+                state_dtype: int = KDA_DTYPE_F32, weight_part_stride: int = 0,
+                cache_index_stride: int = 0) -> KdaConvLayout:
+    """A version-1 layout; weight_part_stride 0 = one (dim, 4) weight array,
+    cache_index_stride 0 = contiguous cache indices."""
     return KdaConvLayout(x_dtype, state_width, (ctypes.c_int64 * 3)(*state_stride),
-                         (ctypes.c_int64 * 2)(*weight_stride), state_dtype, 0)
+                         (ctypes.c_int64 * 2)(*weight_stride), state_dtype, 1,
+                         weight_part_stride, cache_index_stride)
 
 
 class KdaL2Norm(ctypes.Structure):
@@ -217,12 +223,14 @@ def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: tor
                          l2norm_eps: float = 1e-6) -> torch.Tensor:
     """One decode step: x (batch, dim), row i the next token of the sequence at
     conv-state line cache_indices[i].  Returns (dim // part_dim, batch, part_dim)
-    in x's dtype and shifts each touched line by one row, in place.
-    `use_qk_l2norm` as for packed_causal_conv1d_fn."""
+    in x's dtype and shifts each touched line by one row, in place.  The
+    weight may be (dim, 4) or the kda_decode page's (dim // part_dim, 4,
+    part_dim) [qkv, width, channel] form, with any strides; cache_indices may
+    be a strided 1-D view.  `use_qk_l2norm` as for packed_causal_conv1d_fn."""
     act = activation_code(activation)
     _check_conv_tensors(x, weight, bias, conv_states, out, part_dim, x.size(0) if x.dim() else 0)
     batch, dim = x.shape
-    _check_vector("cache_indices", cache_indices, batch, (torch.int32,))
+    _check_vector("cache_indices", cache_indices, batch, (torch.int32,), strided=True)
     _check_devices(x=x, weight=weight, bias=bias, conv_states=conv_states,
                    cache_indices=cache_indices, out=out)
     if out is None:
@@ -230,8 +238,8 @@ def causal_conv1d_update(x: torch.Tensor, conv_states: torch.Tensor, weight: tor
     null = -(2 ** 62) if null_block_id is None else int(null_block_id)
     norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
     kda_conv1d_update_l2norm(x, x.stride(0), batch, dim, part_dim, weight, bias, conv_states,
-                             cache_indices, null, act, out, layout_of(x, weight, conv_states),
-                             norm, stream)
+                             cache_indices, null, act, out,
+                             layout_of(x, weight, conv_states, cache_indices), norm, stream)
     return out
 
 
@@ -316,30 +324,45 @@ _DTYPES = {torch.bfloat16: KDA_DTYPE_BF16, torch.float16: KDA_DTYPE_F16,
 _STATE_DTYPES = {torch.float32: KDA_DTYPE_F32, torch.bfloat16: KDA_DTYPE_BF16}
 
 
+def _weight_shape_ok(weight: torch.Tensor, dim: int, part_dim: int) -> bool:
+    """A (dim, 4) weight, or the kda_decode page's [qkv, width, channel] form
+    (dim / part_dim, 4, part_dim); fp32, any strides."""
+    if weight.dtype != torch.float32:
+        return False
+    if weight.dim() == 2:
+        return tuple(weight.shape) == (dim, 4)
+    return (weight.dim() == 3 and part_dim > 0 and dim % part_dim == 0
+            and tuple(weight.shape) == (dim // part_dim, 4, part_dim))
+
+
 def packed_causal_conv1d_supported(x: torch.Tensor, weight: torch.Tensor,
                                    conv_states: torch.Tensor, part_dim: int) -> bool:
     """Whether packed_causal_conv1d_fn takes these inputs: the page's predicate
     (x CUDA, 2-D, unit channel stride, bf16 / fp16 / fp32; FP32 weight (dim, 4)
     and conv_states (lines, dim, >= 3), any strides; part_dim a multiple of 64
     dividing dim) plus this library's alignment rules (x rows on 16-byte
-    boundaries, state width at most 64), widened to a bf16 conv state."""
+    boundaries, state width at most 64), widened to a bf16 conv state and to
+    the kda_decode page's (dim / part_dim, 4, part_dim) weight."""
     if not (x.is_cuda and x.dim() == 2 and x.stride(1) == 1 and x.dtype in _DTYPES):
         return False
     quantum = 4 if x.dtype == torch.float32 else 8
     return (
         x.stride(0) % quantum == 0 and x.data_ptr() % 16 == 0
-        and weight.dtype == torch.float32 and weight.dim() == 2
-        and weight.size(0) == x.size(1) and weight.size(1) == 4
+        and _weight_shape_ok(weight, x.size(1), part_dim)
         and conv_states.dtype in _STATE_DTYPES and conv_states.dim() == 3
         and conv_states.size(1) == x.size(1) and 3 <= conv_states.size(2) <= 64
         and part_dim > 0 and part_dim % 64 == 0 and x.size(1) % part_dim == 0
     )
 
 
-def _check_vector(name: str, t: torch.Tensor, need: int, dtypes: tuple) -> None:
+def _check_vector(name: str, t: torch.Tensor, need: int, dtypes: tuple,
+                  strided: bool = False) -> None:
     if t.dtype not in dtypes:
         raise TypeError(f"{name} must be {' or '.join(str(d) for d in dtypes)}, not {t.dtype}")
-    if t.dim() != 1 or not t.is_contiguous():
+    if strided:
+        if t.dim() != 1 or (t.numel() > 1 and t.stride(0) < 1):
+            raise ValueError(f"{name} must be a 1-D tensor with a positive stride")
+    elif t.dim() != 1 or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous 1-D tensor")
     if t.numel() < need:
         raise ValueError(f"{name} has {t.numel()} entries, {need} needed")
@@ -353,8 +376,9 @@ def _check_conv_tensors(x, weight, bias, conv_states, out, part_dim: int, rows: 
     if x.dtype not in _DTYPES:
         raise TypeError(f"x must be bf16, fp16 or fp32, not {x.dtype}")
     dim = x.size(1)
-    if weight.dtype != torch.float32 or tuple(weight.shape) != (dim, 4):
-        raise ValueError(f"weight must be fp32 ({dim}, 4), not {weight.dtype} {tuple(weight.shape)}")
+    if not _weight_shape_ok(weight, dim, part_dim):
+        raise ValueError(f"weight must be fp32 ({dim}, 4) or (parts, 4, part_dim), not "
+                         f"{weight.dtype} {tuple(weight.shape)}")
     if bias is not None and (bias.dtype != torch.float32 or tuple(bias.shape) != (dim,)
                              or not bias.is_contiguous()):
         raise ValueError(f"bias must be a contiguous fp32 ({dim},) tensor or None")
@@ -379,12 +403,20 @@ def _check_devices(**tensors) -> None:
             raise ValueError(f"{name} is on {t.device}, x on {dev}")
 
 
-def layout_of(x: torch.Tensor, weight: torch.Tensor, conv_states: torch.Tensor) -> KdaConvLayout:
-    """The kda_conv_layout_t describing these tensors."""
+def layout_of(x: torch.Tensor, weight: torch.Tensor, conv_states: torch.Tensor,
+              cache_indices: torch.Tensor | None = None) -> KdaConvLayout:
+    """The kda_conv_layout_t describing these tensors.  A 3-D weight is the
+    (parts, 4, part_dim) [qkv, width, channel] form."""
     if conv_states.dtype not in _STATE_DTYPES:
         raise TypeError(f"conv_states must be fp32 or bf16, not {conv_states.dtype}")
-    return make_layout(_DTYPES[x.dtype], conv_states.size(2), conv_states.stride(),
-                       weight.stride(), _STATE_DTYPES[conv_states.dtype])
+    if weight.dim() == 3:
+        w_stride, w_part = (weight.stride(2), weight.stride(1)), weight.stride(0)
+    else:
+        w_stride, w_part = weight.stride(), 0
+    ci_stride = cache_indices.stride(0) if cache_indices is not None and cache_indices.numel() > 1 \
+        else 0
+    return make_layout(_DTYPES[x.dtype], conv_states.size(2), conv_states.stride(), w_stride,
+                       _STATE_DTYPES[conv_states.dtype], w_part, ci_stride)
 
 
 def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.Tensor | None,
@@ -395,6 +427,10 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
                             use_qk_l2norm: bool = False, head_dim: int = 128,
                             l2norm_eps: float = 1e-6) -> torch.Tensor:
     """Varlen causal depthwise conv of x (tokens, dim), dim = parts x part_dim.
+
+    weight is (dim, 4) fp32 or (parts, 4, part_dim) (the kda_decode page's
+    [qkv, width, channel] copy), any strides; cache_indices may be a strided
+    1-D view (the page passes its stride to the kernel).
 
     Returns (dim // part_dim, tokens, part_dim) in x's dtype; conv_states is
     updated in place.  `activation` "silu", "swish" or True selects SiLU;
@@ -407,7 +443,7 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
     tokens, dim = x.shape
     num_seqs = max(query_start_loc.numel() - 1, 0)
     _check_vector("query_start_loc", query_start_loc, 0, (torch.int32,))
-    _check_vector("cache_indices", cache_indices, num_seqs, (torch.int32,))
+    _check_vector("cache_indices", cache_indices, num_seqs, (torch.int32,), strided=True)
     _check_vector("has_initial_state", has_initial_state, num_seqs, (torch.bool, torch.uint8))
     _check_devices(x=x, weight=weight, bias=bias, conv_states=conv_states,
                    query_start_loc=query_start_loc, cache_indices=cache_indices,
@@ -418,6 +454,6 @@ def packed_causal_conv1d_fn(x: torch.Tensor, weight: torch.Tensor, bias: torch.T
     norm = make_l2norm(0b011, head_dim, l2norm_eps) if use_qk_l2norm else None
     kda_packed_conv1d_l2norm(x, x.stride(0), tokens, dim, part_dim, weight, bias, conv_states,
                              cache_indices, has_initial_state, query_start_loc,
-                             num_seqs, null, act, out, layout_of(x, weight, conv_states),
-                             norm, stream)
+                             num_seqs, null, act, out,
+                             layout_of(x, weight, conv_states, cache_indices), norm, stream)
     return out

@@ -30,6 +30,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <float.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -96,8 +98,9 @@ struct Params {
     int part_dim;
     int num_seqs;
     const float *weight;
-    int64_t w_stride_c;  // weight[c][j] at weight[c * w_stride_c + j * w_stride_j]
-    int64_t w_stride_j;
+    int64_t w_stride_c;  // weight[c][j] at weight[(c / part_dim) * w_stride_part +
+    int64_t w_stride_j;  //   (c % part_dim) * w_stride_c + j * w_stride_j]
+    int64_t w_stride_part;
     bool weight_dense;  // strides (4, 1): one float4 per channel
     const float *bias;
     void *conv_states;    // fp32, or bf16 when state_bf16
@@ -111,6 +114,7 @@ struct Params {
     bool weight_tapvec;   // tap-major weight (w_stride_c == 1, w_stride_j % 4 == 0,
                           // 16-byte base): a tap's four channels are one float4
     const int32_t *cache_indices;
+    int64_t ci_stride;  // sequence s uses cache_indices[s * ci_stride]
     const uint8_t *has_initial_state;
     const int32_t *qsl;
     int64_t null_block_id;
@@ -121,6 +125,8 @@ struct Params {
     int64_t total_warps;   // programs * warps_per_prog
     int search_steps;      // radix-32 levels: smallest s with 32^s >= num_seqs
     int search_top;        // 32^(search_steps - 1)
+    int win_span;          // ceil(tokens / chunk): the owner of program p is >= p - win_span
+    int win_rounds;        // 32-entry rounds of the window search (0: the radix search)
     uint32_t norm_mask;    // planes whose heads are L2-normalised (kNorm kernels)
     int norm_lanes;        // lanes per head: head_dim / VEC (a power of two <= 32)
     float norm_eps;        // added to the sum of squares inside the root
@@ -330,6 +336,13 @@ __device__ __forceinline__ void state_set4(const Params &p, int64_t i, bool bf16
             make_float4(v[0], v[1], v[2], v[3]);
 }
 
+// Element offset of weight[c][0] (c's part, then c within the part).  A
+// thread's VEC channels never straddle a part (part_dim % 64 == 0, c % VEC == 0).
+__device__ __forceinline__ int64_t weight_base(const Params &p, int c) {
+    const int part = c / p.part_dim;
+    return (int64_t)part * p.w_stride_part + (int64_t)(c - part * p.part_dim) * p.w_stride_c;
+}
+
 // Conv state element i (any layout), fp32 or bf16.
 __device__ __forceinline__ float state_get(const Params &p, int64_t i) {
     if (p.state_bf16)
@@ -516,6 +529,54 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
     return base;
 }
 
+// Entry r of v for a warp-uniform r (a chain of selects, no local memory).
+template <int N>
+__device__ __forceinline__ int pick(const int (&v)[N], int r) {
+    int x = v[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) x = (r == i) ? v[i] : x;
+    return x;
+}
+
+// The same search in one round of loads.  With 0 <= qsl[s] <= tokens,
+// f(s) <= prog < f(s+1) puts s in [prog - floor(tokens / chunk), prog], and
+// the last sequence's programs end before ceil(tokens / chunk) + num_seqs, so
+// s >= prog - ceil(tokens / chunk) holds for every owner s.  Hence
+// the warp loads that window of query_start_loc (with the entry after it) at
+// once, 32 entries per round and up to kMaxRounds rounds, all independent,
+// instead of a chain of dependent levels.  floor(q / chunk) + j <= prog is
+// tested as q < (prog - j + 1) * chunk (no division).  *q0 and *q1 receive
+// qsl[s] and qsl[s+1] from the loaded window.  Returns -1 for an idle program.
+template <int kMaxRounds>
+__device__ __forceinline__ int find_sequence_window(const Params &p, int prog, int lane, int &q0,
+                                                    int &q1) {
+    const int lo = max(0, prog - p.win_span);
+    const int hi = min(p.num_seqs, prog + 1);  // entries lo .. hi are loaded; s < hi
+    int v[kMaxRounds];
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        const int j = lo + 32 * r + lane;
+        v[r] = 0;
+        if (r < p.win_rounds && j <= hi) v[r] = __ldg(p.qsl + j);
+    }
+    int count = 0;
+#pragma unroll
+    for (int r = 0; r < kMaxRounds; ++r) {
+        if (r < p.win_rounds) {
+            const int j = lo + 32 * r + lane;
+            const bool ok = j < hi && (int64_t)v[r] < (int64_t)(prog - j + 1) * p.chunk;
+            count += __popc(__ballot_sync(0xFFFFFFFFu, ok));
+        }
+    }
+    if (count == 0) return -1;
+    const int i0 = count - 1, i1 = count;  // window positions of s and s + 1
+    q0 = __shfl_sync(0xFFFFFFFFu, pick(v, i0 >> 5), i0 & 31);
+    q1 = __shfl_sync(0xFFFFFFFFu, pick(v, i1 >> 5), i1 & 31);
+    return lo + i0;
+}
+
+constexpr int kWindowRounds = 4;  // the window search covers up to 128 entries
+
 // A hint to the TMA unit: bring `bytes` of global memory (16-byte aligned, a
 // multiple of 16 bytes) into L2.  It holds no register and nothing waits on it.
 __device__ __forceinline__ void l2_prefetch(const void *ptr, uint32_t bytes) {
@@ -573,15 +634,22 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
     const int prog = (int)(gwarp / p.warps_per_prog);
     const int wv = (int)(gwarp - (int64_t)prog * p.warps_per_prog);
 
-    const int s = find_sequence(p, prog, lane);
-    if (s < 0) return;
-    const int q0 = __ldg(p.qsl + s);
+    int s, q0, q1;
+    if (p.win_rounds > 0) {
+        s = find_sequence_window<kWindowRounds>(p, prog, lane, q0, q1);
+        if (s < 0) return;
+    } else {
+        s = find_sequence(p, prog, lane);
+        if (s < 0) return;
+        q0 = __ldg(p.qsl + s);
+        q1 = __ldg(p.qsl + s + 1);
+    }
     const int f_s = q0 / p.chunk + s;
     if (f_s > prog) return;
     // Clamp the sequence to [0, tokens) so that malformed offsets never read or
     // write outside x / out.
     const int a = max(q0, 0);
-    const int e = min(__ldg(p.qsl + s + 1), p.tokens);
+    const int e = min(q1, p.tokens);
     const int k = prog - f_s;
     const int64_t t0_wide = (int64_t)a + (int64_t)k * p.chunk;
     if (t0_wide >= e) return;
@@ -603,11 +671,12 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
             w[v][3] = q.w;
         }
     } else {
+        const int64_t wb = weight_base(p, c);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                w[v][j] = __ldg(p.weight + (int64_t)(c + v) * p.w_stride_c + j * p.w_stride_j);
+                w[v][j] = __ldg(p.weight + wb + v * p.w_stride_c + j * p.w_stride_j);
         }
     }
     float bias[VEC];
@@ -638,7 +707,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
     // History rows -3, -2, -1 relative to t0 (h0 oldest), in FP32.
     float h0[VEC], h1[VEC], h2[VEC];
     if (k == 0) {
-        const int64_t line = __ldg(p.cache_indices + s);
+        const int64_t line = __ldg(p.cache_indices + (int64_t)s * p.ci_stride);
         const bool live = line != p.null_block_id;
         const bool read = live && __ldg(p.has_initial_state + s) != 0;
         const int len = e - a;
@@ -872,12 +941,13 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
         }
     } else if (kLayout >= 3) {
         // tap-major: tap j of channels c .. c+3 is one float4
+        const int64_t wb = weight_base(p, c);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int i = 0; i < VEC / 4; ++i) {
                 const float4 q = __ldg(reinterpret_cast<const float4 *>(
-                    p.weight + (int64_t)j * p.w_stride_j + c + 4 * i));
+                    p.weight + wb + (int64_t)j * p.w_stride_j + 4 * i));
                 w[4 * i][j] = q.x;
                 w[4 * i + 1][j] = q.y;
                 w[4 * i + 2][j] = q.z;
@@ -885,11 +955,12 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
             }
         }
     } else {
+        const int64_t wb = weight_base(p, c);
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                w[v][j] = __ldg(p.weight + (int64_t)(c + v) * p.w_stride_c + j * p.w_stride_j);
+                w[v][j] = __ldg(p.weight + wb + v * p.w_stride_c + j * p.w_stride_j);
         }
     }
     float bias[VEC];
@@ -908,7 +979,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
     float xv[VEC];
     widen<VEC, kDtype>(raw, xv);
 
-    const int64_t line = __ldg(p.cache_indices + token);
+    const int64_t line = __ldg(p.cache_indices + token * p.ci_stride);
     const bool live = line != p.null_block_id;
     float h0[VEC], h1[VEC], h2[VEC];
     if (kLayout < 2 || p.state_dense) {
@@ -1061,8 +1132,31 @@ kda_conv_layout_t default_layout(int64_t dim) {
     l.weight_stride[0] = 4;
     l.weight_stride[1] = 1;
     l.state_dtype = KDA_DTYPE_F32;
-    l.reserved = 0;
+    l.version = 0;
+    l.weight_part_stride = 0;
+    l.cache_index_stride = 0;
     return l;
+}
+
+// The caller's layout (NULL: the default).  A version-0 struct may be the
+// shorter struct of earlier releases, so the version-1 fields are read only
+// when the caller says they are there.
+kda_conv_layout_t read_layout(const kda_conv_layout_t *in, int64_t dim) {
+    if (!in) return default_layout(dim);
+    kda_conv_layout_t l;
+    memcpy(&l, in, offsetof(kda_conv_layout_t, weight_part_stride));
+    l.weight_part_stride = 0;
+    l.cache_index_stride = 0;
+    if (l.version == 1) {
+        l.weight_part_stride = in->weight_part_stride;
+        l.cache_index_stride = in->cache_index_stride;
+    }
+    return l;
+}
+
+// Element stride between weight parts: the layout's, or that of one (dim, 4) array.
+int64_t weight_part_stride(const kda_conv_layout_t &l, int64_t part_dim) {
+    return l.weight_part_stride != 0 ? l.weight_part_stride : part_dim * l.weight_stride[0];
 }
 
 kda_status_t check_sizes(int64_t x_row_stride, int64_t tokens, int64_t dim, int64_t part_dim,
@@ -1088,13 +1182,17 @@ bool state_is_posvec(const kda_conv_layout_t &l, const void *conv_states) {
            aligned(conv_states, vec_bytes);
 }
 
-// Tap-major weight whose four-channel groups of a tap are aligned float4s.
-bool weight_is_tapvec(const kda_conv_layout_t &l, const float *weight) {
-    return l.weight_stride[0] == 1 && l.weight_stride[1] % 4 == 0 && aligned(weight, 16);
+// Tap-major weight whose four-channel groups of a tap are aligned float4s
+// (also a [part, tap, channel] weight with such strides).
+bool weight_is_tapvec(const kda_conv_layout_t &l, const float *weight, int64_t part_dim) {
+    return l.weight_stride[0] == 1 && l.weight_stride[1] % 4 == 0 &&
+           weight_part_stride(l, part_dim) % 4 == 0 && aligned(weight, 16);
 }
 
-bool weight_is_dense(const kda_conv_layout_t &l) {
-    return l.weight_stride[0] == 4 && l.weight_stride[1] == 1;
+// One (dim, 4) contiguous array: one float4 per channel.
+bool weight_is_dense(const kda_conv_layout_t &l, int64_t part_dim) {
+    return l.weight_stride[0] == 4 && l.weight_stride[1] == 1 &&
+           weight_part_stride(l, part_dim) == 4 * part_dim;
 }
 
 kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int64_t dim,
@@ -1108,7 +1206,8 @@ kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int
     if (activation != KDA_ACT_NONE && activation != KDA_ACT_SILU) return KDA_ERR_INVALID_ARG;
     if (l.x_dtype != KDA_DTYPE_BF16 && l.x_dtype != KDA_DTYPE_F16 && l.x_dtype != KDA_DTYPE_F32)
         return KDA_ERR_INVALID_ARG;
-    if ((l.state_dtype != KDA_DTYPE_F32 && l.state_dtype != KDA_DTYPE_BF16) || l.reserved != 0)
+    if ((l.state_dtype != KDA_DTYPE_F32 && l.state_dtype != KDA_DTYPE_BF16) ||
+        (l.version != 0 && l.version != 1) || l.cache_index_stride < 0)
         return KDA_ERR_INVALID_ARG;
     if (l.state_width < 3) return KDA_ERR_INVALID_ARG;
     if (l.state_width > kMaxStateWidth) return KDA_ERR_UNSUPPORTED;
@@ -1120,7 +1219,8 @@ kda_status_t check_args(const void *x, int64_t x_row_stride, int64_t tokens, int
     if (!aligned(x, 16) || x_row_stride % row_quantum != 0 || !aligned(out, 16) ||
         (bias && !aligned(bias, 16)))
         return KDA_ERR_MISALIGNED;
-    if (weight_is_dense(l) ? !aligned(weight, 16) : !aligned(weight, 4)) return KDA_ERR_MISALIGNED;
+    if (weight_is_dense(l, part_dim) ? !aligned(weight, 16) : !aligned(weight, 4))
+        return KDA_ERR_MISALIGNED;
     const uintptr_t state_elem = l.state_dtype == KDA_DTYPE_BF16 ? 2 : 4;
     if (!aligned(conv_states, state_is_dense(l, dim) ? 16 : state_elem)) return KDA_ERR_MISALIGNED;
     return KDA_OK;
@@ -1136,13 +1236,24 @@ struct Shape {
     bool short_seqs;  // mean sequence length below kShortMean: the kShort kernel
 };
 
-// Chunk length.  The resident-warp budget is waves x SMs x warps per SM.
-// Preferred: the smallest multiple of the queue depth for which every program
-// (ceil(tokens/chunk) + num_seqs of them, the slack ones included) fits in the
-// budget at once, so no CTA waits for a later wave.  When num_seqs alone
-// exceeds the budget, the chunk that spreads the tokens over the budget.
-// Clamped to [kMinChunk, kMaxChunk].  It depends only on the scalar sizes and
-// the SM count, so a captured launch stays valid for new metadata.
+// Chunk length (rows per program), rounded up to a multiple of the queue
+// depth and clamped to [kMinChunk, kMaxChunk].  The resident-warp budget
+// (slots) is waves x SMs x warps per SM.
+//   * One sequence: the smallest chunk for which every program fits in the
+//     budget at once, so no CTA waits for a later wave.
+//   * num_seqs at or above the budget's program count: the even spread of the
+//     tokens over the budget.
+//   * In between: the one-wave fit, but at most the even spread over two
+//     waves (no less than kSpreadFloor rows).  The one-wave fit alone gives
+//     tokens / (budget - num_seqs) rows, which grows without bound as num_seqs
+//     nears the budget: one long prompt among ~100 short ones then streamed
+//     through a few latency-bound warps (GB300, 16K tokens: one 8192-token
+//     prompt among 99 of 80 tokens took 152 us with 900-row chunks and 58 us
+//     with 72-row ones; batches of uniform sequences keep their time).
+// It depends only on the scalar sizes and the SM count, so a captured launch
+// stays valid for new metadata.
+constexpr int64_t kSpreadFloor = 48;
+
 Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
                    int blocks_per_sm = KDA_MIN_BLOCKS) {
     Shape sh{};
@@ -1154,6 +1265,11 @@ Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
     int64_t chunk;
     if (max_programs > num_seqs) {
         chunk = (tokens + (max_programs - num_seqs) - 1) / (max_programs - num_seqs);
+        if (num_seqs > 1) {
+            int64_t spread2 = (tokens * sh.warps_per_prog + 2 * slots - 1) / (2 * slots);
+            if (spread2 < kSpreadFloor) spread2 = kSpreadFloor;
+            if (chunk > spread2) chunk = spread2;
+        }
     } else {
         chunk = (tokens * sh.warps_per_prog + slots - 1) / slots;
     }
@@ -1277,6 +1393,9 @@ kda_status_t check_norm(const kda_l2norm_t *norm, int64_t dim, int64_t part_dim)
     if (!norm || norm->plane_mask == 0u) return KDA_OK;
     if (norm->reserved != 0) return KDA_ERR_INVALID_ARG;
     if (!(norm->eps >= 0.0f) || norm->eps > 3.0e38f) return KDA_ERR_INVALID_ARG;  // NaN too
+    // A subnormal eps would be flushed by the SFU root (rsqrt.approx.ftz) and
+    // leave a head of tiny activations inf or NaN: 0 or a normal number only.
+    if (norm->eps > 0.0f && norm->eps < FLT_MIN) return KDA_ERR_INVALID_ARG;
     const int64_t planes = dim / part_dim;
     if (planes < 32 && (norm->plane_mask >> planes) != 0u) return KDA_ERR_INVALID_ARG;
     const int64_t hd = norm->head_dim;
@@ -1300,7 +1419,7 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
                  const int32_t *query_start_loc, int64_t num_seqs, int64_t null_block_id,
                  int activation, void *out, bool preact, const kda_conv_layout_t *layout,
                  const kda_l2norm_t *norm, kda_stream_t stream) {
-    const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
+    const kda_conv_layout_t l = read_layout(layout, dim);
     kda_status_t st = check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
                                  cache_indices, has_initial_state, query_start_loc, num_seqs,
                                  activation, out, l);
@@ -1324,7 +1443,8 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.weight = weight;
     p.w_stride_c = l.weight_stride[0];
     p.w_stride_j = l.weight_stride[1];
-    p.weight_dense = weight_is_dense(l);
+    p.w_stride_part = weight_part_stride(l, part_dim);
+    p.weight_dense = weight_is_dense(l, part_dim);
     p.bias = bias;
     p.conv_states = conv_states;
     p.state_width = l.state_width;
@@ -1332,8 +1452,9 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.state_dense = state_is_dense(l, dim);
     p.state_bf16 = l.state_dtype == KDA_DTYPE_BF16;
     p.state_posvec = state_is_posvec(l, conv_states);
-    p.weight_tapvec = weight_is_tapvec(l, weight);
+    p.weight_tapvec = weight_is_tapvec(l, weight, part_dim);
     p.cache_indices = cache_indices;
+    p.ci_stride = l.cache_index_stride > 0 ? l.cache_index_stride : 1;
     p.has_initial_state = has_initial_state;
     p.qsl = query_start_loc;
     p.null_block_id = null_block_id;
@@ -1350,6 +1471,16 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     }
     p.search_steps = steps;
     p.search_top = steps > 0 ? (int)(reach / 32) : 1;
+    // The window search replaces two or more radix levels when its entries
+    // (ceil(tokens / chunk) + 2 at most) fit in kWindowRounds rounds.  Measured
+    // on GB300: 256 short prefills + 1024 decode tokens 82.8 against 85.1 us,
+    // 1024 decode tokens 33.3 against 33.8 us; with 8 rounds it was slower
+    // than the radix search, and with one level to replace no faster.
+    p.win_span = (int)((tokens + sh.chunk - 1) / sh.chunk);
+    const int64_t win_entries = p.win_span + 2;
+    p.win_rounds = (num_seqs > 32 && win_entries <= 32 * kWindowRounds)
+                       ? (int)((win_entries + 31) / 32)
+                       : 0;
     set_norm(p, preact ? nullptr : norm);
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1422,7 +1553,7 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
                         void *conv_states, const int32_t *cache_indices, int64_t null_block_id,
                         int activation, void *out, const kda_conv_layout_t *layout,
                         const kda_l2norm_t *norm, kda_stream_t stream) {
-    const kda_conv_layout_t l = layout ? *layout : default_layout(dim);
+    const kda_conv_layout_t l = read_layout(layout, dim);
     kda_status_t st = check_args(x, x_row_stride, batch, dim, part_dim, weight, bias, conv_states,
                                  cache_indices, nullptr, nullptr, batch, activation, out, l,
                                  false);
@@ -1442,7 +1573,8 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     p.weight = weight;
     p.w_stride_c = l.weight_stride[0];
     p.w_stride_j = l.weight_stride[1];
-    p.weight_dense = weight_is_dense(l);
+    p.w_stride_part = weight_part_stride(l, part_dim);
+    p.weight_dense = weight_is_dense(l, part_dim);
     p.bias = bias;
     p.conv_states = conv_states;
     p.state_width = l.state_width;
@@ -1450,8 +1582,9 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     p.state_dense = state_is_dense(l, dim);
     p.state_bf16 = l.state_dtype == KDA_DTYPE_BF16;
     p.state_posvec = state_is_posvec(l, conv_states);
-    p.weight_tapvec = weight_is_tapvec(l, weight);
+    p.weight_tapvec = weight_is_tapvec(l, weight, part_dim);
     p.cache_indices = cache_indices;
+    p.ci_stride = l.cache_index_stride > 0 ? l.cache_index_stride : 1;
     p.null_block_id = null_block_id;
     p.out = out;
     p.plane_stride = batch * part_dim;
@@ -1559,7 +1692,7 @@ kda_status_t kda_packed_conv1d_ex_check_args(
     const kda_conv_layout_t *layout) {
     return check_args(x, x_row_stride, tokens, dim, part_dim, weight, bias, conv_states,
                       cache_indices, has_initial_state, query_start_loc, num_seqs, activation,
-                      out, layout ? *layout : default_layout(dim));
+                      out, read_layout(layout, dim));
 }
 
 kda_status_t kda_l2norm_check(const kda_l2norm_t *norm, int64_t dim, int64_t part_dim) {

@@ -164,9 +164,9 @@ def test_validate_metadata(kda):
 
 
 def _layout(kda, dtype=0, width=3, sstride=(3 * 4608, 3, 1), wstride=(4, 1), sdtype=2,
-            reserved=0):
-    lay = kda.make_layout(dtype, width, sstride, wstride, sdtype)
-    lay.reserved = reserved
+            version=1, wpart=0, ci_stride=0):
+    lay = kda.make_layout(dtype, width, sstride, wstride, sdtype, wpart, ci_stride)
+    lay.version = version
     return lay
 
 
@@ -188,7 +188,17 @@ def _layout(kda, dtype=0, width=3, sstride=(3 * 4608, 3, 1), wstride=(4, 1), sdt
     ({"sdtype": 0}, {}, 0),  # bf16 conv state
     ({"sdtype": 1}, {}, 1),  # fp16 conv state: not offered
     ({"sdtype": 3}, {}, 1),
-    ({"reserved": 1}, {}, 1),
+    ({"version": 2}, {}, 1),
+    ({"version": -1}, {}, 1),
+    ({"version": 0, "ci_stride": -5}, {}, 0),  # version 0: the version-1 fields are not read
+    ({"ci_stride": -1}, {}, 1),
+    ({"ci_stride": 3}, {}, 0),
+    # the kda_decode page's [qkv, width, channel] weight: strided, 4-byte alignment
+    ({"wstride": (1, 1536), "wpart": 4 * 1536}, {"weight": A16 + 4}, 0),
+    # (4, 1) with the part stride of one (dim, 4) array is dense: 16-byte alignment
+    ({"wpart": 4 * 1536}, {"weight": A16 + 4}, 3),
+    # (4, 1) with a padded part stride is not one array: 4-byte alignment
+    ({"wpart": 4 * 1536 + 4}, {"weight": A16 + 4}, 0),
     ({"sdtype": 0}, {"conv_states": A16 + 8}, 3),  # dense bf16 state: 16-byte alignment
     ({"sdtype": 0, "sstride": (3 * 4608, 1, 4608)}, {"conv_states": A16 + 2}, 0),
     ({"sdtype": 0, "width": 4, "sstride": (4 * 4608, 4, 1)}, {"conv_states": A16 + 2}, 0),
@@ -214,10 +224,51 @@ def test_layout_struct_matches_the_header(kda):
     """kda_conv_layout_t: two int32, five int64, two int32 (56 bytes, no padding)."""
     import ctypes
 
-    assert ctypes.sizeof(kda.KdaConvLayout) == 56
+    assert ctypes.sizeof(kda.KdaConvLayout) == 72
     assert kda.KdaConvLayout.state_dtype.offset == 48
+    assert kda.KdaConvLayout.version.offset == 52
+    assert kda.KdaConvLayout.weight_part_stride.offset == 56
+    assert kda.KdaConvLayout.cache_index_stride.offset == 64
     lay = kda.make_layout(0, 3, (9, 3, 1), (4, 1))
-    assert lay.state_dtype == kda.KDA_DTYPE_F32 and lay.reserved == 0
+    assert lay.state_dtype == kda.KDA_DTYPE_F32 and lay.version == 1
+    assert lay.weight_part_stride == 0 and lay.cache_index_stride == 0
+
+
+def test_version0_layout_is_read_as_the_shorter_struct(kda):
+    """A caller built against the 56-byte struct (version 0, no part or
+    cache-index stride) is read without touching the bytes after it: the
+    struct is placed at the very end of a page-sized buffer's used part, and
+    whatever follows it (here: a poison pattern) is ignored."""
+    import ctypes
+
+    class Old(ctypes.Structure):
+        _fields_ = [("x_dtype", ctypes.c_int32), ("state_width", ctypes.c_int32),
+                    ("state_stride", ctypes.c_int64 * 3), ("weight_stride", ctypes.c_int64 * 2),
+                    ("state_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    buf = (ctypes.c_uint8 * 72)(*([0] * 56 + [0xFF] * 16))  # poison after the old struct
+    old = Old.from_buffer(buf)
+    old.x_dtype, old.state_width, old.state_dtype, old.reserved = 0, 3, 2, 0
+    old.state_stride[:] = (3 * 4608, 3, 1)
+    old.weight_stride[:] = (4, 1)
+    a = good_args()
+    st = kda.check_args_ex(a["x"], a["x_row_stride"], a["tokens"], a["dim"], a["part_dim"],
+                           a["weight"], a["bias"], a["conv_states"], a["cache_indices"],
+                           a["has_initial_state"], a["query_start_loc"], a["num_seqs"],
+                           a["activation"], a["out"],
+                           ctypes.cast(ctypes.pointer(old), ctypes.POINTER(kda.KdaConvLayout)).contents)
+    assert st == 0  # a poisoned cache-index stride (-1) would be rejected
+
+
+def test_layout_of_reads_the_decode_weight_and_index_strides(kda):
+    x = torch.zeros(8, 192, dtype=torch.bfloat16)
+    w3 = torch.zeros(3, 4, 64)  # [qkv, width, channel]
+    ci = torch.zeros(10, dtype=torch.int32)[::2]
+    lay = kda.layout_of(x, w3, torch.zeros(2, 192, 3), ci)
+    assert tuple(lay.weight_stride) == (1, 64) and lay.weight_part_stride == 256
+    assert lay.cache_index_stride == 2 and lay.version == 1
+    lay = kda.layout_of(x, torch.zeros(192, 4), torch.zeros(2, 192, 3))
+    assert tuple(lay.weight_stride) == (4, 1) and lay.weight_part_stride == 0
 
 
 def test_layout_of_maps_the_state_dtype(kda):
@@ -250,6 +301,9 @@ def test_supported_predicate_rejects_host_tensors(kda):
     (0b011, 128, -1e-6, 4608, 1536, 1),
     (0b011, 128, float("nan"), 4608, 1536, 1),
     (0b011, 128, float("inf"), 4608, 1536, 1),
+    (0b011, 128, 1e-40, 4608, 1536, 1),  # subnormal: flushed by the SFU root
+    (0b011, 128, 1.1754944e-38, 4608, 1536, 0),  # FLT_MIN
+    (0b011, 128, 1e-30, 4608, 1536, 0),
     (0, 7, -5.0, 4608, 1536, 0),  # empty mask: no norm, nothing else checked
 ])
 def test_l2norm_checks(kda, mask, head_dim, eps, dim, part_dim, status):
@@ -269,3 +323,61 @@ def test_l2norm_struct_matches_the_header(kda):
 
     assert ctypes.sizeof(kda.KdaL2Norm) == 16
     assert kda.KdaL2Norm.eps.offset == 8
+
+
+def test_window_search_model(kda):
+    """Host model of the device's one-round window search: for every program
+    p, the owner s (the largest s with f(s) = floor(qsl[s] / chunk) + s <= p)
+    lies in [p - ceil(tokens / chunk), p], the entry after it is inside the
+    loaded window [lo, min(num_seqs, p + 1)], which holds at most
+    ceil(tokens / chunk) + 2 entries, and counting the window's candidates j
+    that pass q < (p - j + 1) * chunk finds s."""
+    rng = np.random.default_rng(11)
+    for trial in range(150):
+        n = int(rng.integers(1, 400))
+        kind = trial % 3
+        if kind == 0:
+            lens = rng.integers(0, 300, size=n)
+        elif kind == 1:
+            lens = rng.integers(0, 3, size=n)
+        else:
+            lens = np.where(rng.random(n) < 0.02, rng.integers(1000, 9000, size=n),
+                            rng.integers(0, 40, size=n))
+        qsl = np.concatenate([[int(rng.integers(0, 50))], lens]).cumsum()
+        tokens = int(qsl[-1] + rng.integers(0, 20))
+        sh = kda.launch_shape(tokens, 4608, 1536, n)
+        chunk, programs = sh["chunk"], sh["programs"]
+        span = -(-tokens // chunk)
+        f = qsl[:-1] // chunk + np.arange(n)
+        p = np.arange(programs)
+        s = np.searchsorted(f, p, side="right") - 1  # owner, -1 before the first
+        lo, hi = np.maximum(0, p - span), np.minimum(n, p + 1)
+        assert (hi - lo + 1 <= span + 2).all()
+        own = s >= 0
+        assert ((lo <= s) & (s < hi))[own].all(), trial
+        # the counted candidates: j in [lo, hi) with q < (p - j + 1) * chunk
+        for pi in rng.choice(programs, size=min(programs, 40), replace=False):
+            j = np.arange(lo[pi], hi[pi])
+            ok = qsl[j] < (pi - j + 1) * chunk
+            assert (ok == (f[j] <= pi)).all()
+            assert int(ok.sum()) - 1 + lo[pi] == s[pi] or (s[pi] == -1 and not ok.any())
+
+
+def test_chunk_bounded_for_many_sequences(kda):
+    """The chunk stays near the even spread of the tokens over the resident
+    warps whatever the sequence count: with 2..117 sequences at 16K tokens
+    (3 x 1536 channels: 36 warps per program, 118 programs per wave of
+    152 x 7 CTAs) it is the two-wave spread, 72 rows, where the one-wave fit
+    alone would give up to 2048 rows (one long prompt among short ones then
+    streams through a few warps); one sequence keeps the one-wave fit (144
+    rows) and 118 or more take the one-wave spread."""
+    spread2 = -(-16384 * 36 // (2 * 152 * 4 * 7))
+    assert kda.launch_shape(16384, 4608, 1536, 1)["chunk"] == 144
+    for n in range(2, 118):
+        sh = kda.launch_shape(16384, 4608, 1536, n)
+        assert sh["chunk"] == -(-spread2 // 6) * 6 == 72, n
+    for n in (118, 200, 1280):
+        assert kda.launch_shape(16384, 4608, 1536, n)["chunk"] == -(-16384 * 36 // 4256 // 6) * 6
+    # small batches keep the one-wave fit (no less than 48 rows from the cap)
+    assert kda.launch_shape(2430, 4608, 1536, 8)["chunk"] == 24
+    assert kda.launch_shape(2600, 4608, 1536, 31)["chunk"] == 30

@@ -31,10 +31,40 @@ def _lib():
     pkg.lib()
 
 
-def _run_device(b: workloads.Batch, state_mem_order: str = "dense", weight_tap_major=False):
+def weight_to_device(b: workloads.Batch, form, dev):
+    """The weight as a device tensor and its (channel, tap) strides and part
+    stride.  form False / "channel_major": (dim, 4) contiguous; True /
+    "tap_major": (4, dim) memory viewed as (dim, 4); "decode3": the kda_decode
+    page's [qkv, width, channel] buffer, (dim / part_dim, 4, part_dim)."""
+    if form == "decode3":
+        parts = b.dim // b.part_dim
+        w3 = np.ascontiguousarray(b.weight.reshape(parts, b.part_dim, 4).transpose(0, 2, 1))
+        w = torch.from_numpy(w3).to(dev)
+        return w, (w.stride(2), w.stride(1)), w.stride(0)
+    if form is True or form == "tap_major":
+        w = torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t()
+    else:
+        w = torch.from_numpy(b.weight).to(dev)
+    return w, w.stride(), 0
+
+
+def strided_indices(ci: np.ndarray, stride: int, dev) -> torch.Tensor:
+    """cache_indices as a view with `stride` elements between entries; the
+    entries in between hold line 0, so reading one of them is caught."""
+    if stride <= 1:
+        return torch.from_numpy(ci).to(dev)
+    buf = torch.zeros(max(len(ci) * stride, 1), dtype=torch.int32, device=dev)
+    view = buf[::stride][:len(ci)]
+    view.copy_(torch.from_numpy(ci))
+    return view
+
+
+def _run_device(b: workloads.Batch, state_mem_order: str = "dense", weight_tap_major=False,
+                ci_stride: int = 1):
     """Runs kda_packed_conv1d_ex on b.  state_mem_order 'dense' keeps
     conv_states (lines, dim, K) contiguous; 'position_major' stores it as
-    (lines, K, dim) memory viewed as (lines, dim, K)."""
+    (lines, K, dim) memory viewed as (lines, dim, K).  weight_tap_major is a
+    weight_to_device form; ci_stride > 1 passes cache_indices strided."""
     import linear_attention_prefill_varlen_gb300 as pkg
 
     dev = torch.device("cuda")
@@ -51,16 +81,13 @@ def _run_device(b: workloads.Batch, state_mem_order: str = "dense", weight_tap_m
     else:
         st = state_to_device(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1)), dev)
         st = st.transpose(1, 2)
-    if weight_tap_major:
-        w = torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t()
-    else:
-        w = torch.from_numpy(b.weight).to(dev)
+    w, w_strides, w_part = weight_to_device(b, weight_tap_major, dev)
     bias = None if b.bias is None else torch.from_numpy(b.bias).to(dev)
-    meta = [torch.from_numpy(a).to(dev) for a in
-            (b.cache_indices, b.has_initial_state, b.query_start_loc)]
+    meta = [strided_indices(b.cache_indices, ci_stride, dev)] + [
+        torch.from_numpy(a).to(dev) for a in (b.has_initial_state, b.query_start_loc)]
     dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
-    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride(),
-                             state_dtype_of(st))
+    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w_strides,
+                             state_dtype_of(st), w_part, ci_stride if ci_stride > 1 else 0)
     esz = 4 if b.x_dtype == "f32" else 2
     pkg.kda_packed_conv1d_ex(x.data_ptr() + esz * b.col_offset, b.row_stride, b.tokens, b.dim,
                              b.part_dim, w, bias, st, meta[0], meta[1], meta[2], b.num_seqs,
@@ -115,7 +142,8 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("mem", ["dense", "position_major"])
-@pytest.mark.parametrize("tap_major", [False, True], ids=["w_channel_major", "w_tap_major"])
+@pytest.mark.parametrize("tap_major", [False, True, "decode3"],
+                         ids=["w_channel_major", "w_tap_major", "w_qkv_width_channel"])
 def test_general_layout(case, mem, tap_major):
     name, seed, lengths, dim, part_dim, row_stride, col_offset, extra = case
     extra = dict(extra)
@@ -161,5 +189,44 @@ def test_page_style_wrapper_with_fp16_and_wide_state():
     ref_st = b.conv_states.copy()
     ref = pins.run_oracle_ex(b, states=ref_st)
     assert out.dtype == torch.float16
+    assert np.array_equal(state_to_host(st).view(np.uint32), ref_st.view(np.uint32))
+    _compare(b, out.view(torch.int16).cpu().numpy(), ref["out"])
+
+
+@pytest.mark.parametrize("ci_stride", [2, 3, 7])
+@pytest.mark.parametrize("weight", ["channel_major", "decode3"])
+def test_strided_cache_indices(ci_stride, weight):
+    """cache_indices passed as a strided view (the page's launch passes
+    cache_indices.stride(0)): sequence s uses entry s * stride, and the
+    entries in between (line 0) are never read."""
+    b = workloads.make_batch(f"ci_stride{ci_stride}", 420 + ci_stride, [1, 5, 40, 2, 130, 3],
+                             256, 128, 264, 12, col_offset=8, his_p=0.7, null_count=1)
+    st = b.conv_states.copy()
+    ref = pins.run_oracle_ex(b, states=st)
+    got, got_states = _run_device(b, "dense", weight, ci_stride)
+    assert_states_equal(got_states, st)
+    _compare(b, got, ref["out"])
+
+
+def test_page_wrapper_with_the_decode_weight_and_strided_indices():
+    """packed_causal_conv1d_fn given the kda_decode page's (3, 4, part_dim)
+    weight and a strided cache_indices view derives the layout from them."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    b = workloads.make_batch("wrap3", 431, [17, 3, 40, 1], 384, 128, 384, 9, his_p=0.7,
+                             null_count=1)
+    dev = torch.device("cuda")
+    x = torch.from_numpy(b.x_buf.view(np.int16)).to(dev).view(torch.bfloat16)
+    st = state_to_device(b.conv_states, dev)
+    w, _, _ = weight_to_device(b, "decode3", dev)
+    ci = strided_indices(b.cache_indices, 4, dev)
+    assert pkg.packed_causal_conv1d_supported(x, w, st, b.part_dim)
+    meta = [torch.from_numpy(a).to(dev) for a in (b.query_start_loc, b.has_initial_state)]
+    out = pkg.packed_causal_conv1d_fn(x, w, torch.from_numpy(b.bias).to(dev), st, meta[0], ci,
+                                      meta[1].bool(), b.part_dim, activation="silu",
+                                      null_block_id=-1)
+    torch.cuda.synchronize()
+    ref_st = b.conv_states.copy()
+    ref = pins.run_oracle_ex(b, states=ref_st)
     assert np.array_equal(state_to_host(st).view(np.uint32), ref_st.view(np.uint32))
     _compare(b, out.view(torch.int16).cpu().numpy(), ref["out"])

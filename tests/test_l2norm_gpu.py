@@ -156,6 +156,26 @@ def test_l2norm_large_eps_and_zero_heads():
     assert (got[0][:, 32:64].view(np.uint16) == 0).all()
 
 
+def test_l2norm_tiny_heads_stay_finite():
+    """Heads of tiny activations (taps and bias scaled by 2^-70, so that the
+    head's sum of squares is far below FLT_MIN) with eps = 1e-6: the root of
+    (sum + eps) is a normal number, the outputs are finite and match the
+    float64 norm of the oracle."""
+    b = workloads.make_batch("l2tiny", 1112, [5, 17, 40], 256, 128, 264, 6, col_offset=8,
+                             his_p=0.5, null_count=1)
+    b.weight[:64] *= np.float32(2.0 ** -70)
+    b.bias[:64] *= np.float32(2.0 ** -70)
+    b.conv_states[:, :64] = 0.0
+    eps = _eps32(1e-6)
+    st = b.conv_states.copy()
+    want = pins.run_oracle_l2norm(b, 0b11, 32, eps, states=st)["out"]
+    got, got_st = _run(b, 0b11, 32, eps)
+    assert_states_equal(got_st, st)
+    _compare(b, got, want, 0b11)
+    g = got[0][:, :64].view(np.uint16)
+    assert not (((g & 0x7F80) == 0x7F80) & (g != 0xFFFF)).any()  # no inf / NaN written
+
+
 @pytest.mark.parametrize("name", ["long16k", "decode"])
 def test_l2norm_full_size(name):
     """The 16K prefill chunk and the 1024-sequence decode step with q and k

@@ -15,7 +15,7 @@ import pins
 import workloads
 from gpu_helpers import (assert_states_equal, state_dtype_of, state_to_device, state_to_host,
                          ulp_diff)
-from test_general_layout_gpu import _compare
+from test_general_layout_gpu import _compare, strided_indices, weight_to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -36,7 +36,7 @@ def _decode_batch(seed, batch, dim, part_dim, row_stride, lines, **kw):
     return b
 
 
-def _run_update(b, position_major=False, tap_major=False):
+def _run_update(b, position_major=False, tap_major=False, ci_stride=1):
     import linear_attention_prefill_varlen_gb300 as pkg
 
     dev = torch.device("cuda")
@@ -49,13 +49,12 @@ def _run_update(b, position_major=False, tap_major=False):
         st = st.transpose(1, 2)
     else:
         st = state_to_device(b.conv_states, dev)
-    w = (torch.from_numpy(np.ascontiguousarray(b.weight.T)).to(dev).t() if tap_major
-         else torch.from_numpy(b.weight).to(dev))
+    w, w_strides, w_part = weight_to_device(b, tap_major, dev)
     bias = None if b.bias is None else torch.from_numpy(b.bias).to(dev)
-    ci = torch.from_numpy(b.cache_indices).to(dev)
+    ci = strided_indices(b.cache_indices, ci_stride, dev)
     dt = {"bf16": pkg.KDA_DTYPE_BF16, "f16": pkg.KDA_DTYPE_F16, "f32": pkg.KDA_DTYPE_F32}
-    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w.stride(),
-                             state_dtype_of(st))
+    layout = pkg.make_layout(dt[b.x_dtype], st.size(2), st.stride(), w_strides,
+                             state_dtype_of(st), w_part, ci_stride if ci_stride > 1 else 0)
     esz = 4 if f32 else 2
     pkg.kda_conv1d_update(x.data_ptr() + esz * b.col_offset, b.row_stride, b.tokens, b.dim,
                           b.part_dim, w, bias, st, ci, b.null_block_id, b.activation, out, layout)
@@ -80,7 +79,8 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 @pytest.mark.parametrize("position_major", [False, True], ids=["dense", "position_major"])
-@pytest.mark.parametrize("tap_major", [False, True], ids=["w_channel_major", "w_tap_major"])
+@pytest.mark.parametrize("tap_major", [False, True, "decode3"],
+                         ids=["w_channel_major", "w_tap_major", "w_qkv_width_channel"])
 def test_update_matches_oracle(case, position_major, tap_major):
     name, seed, batch, dim, part_dim, row_stride, col_offset, extra = case
     b = _decode_batch(seed, batch, dim, part_dim, row_stride, 2 * batch, col_offset=col_offset,
@@ -274,3 +274,39 @@ def test_update_position_major_state_at_an_unaligned_base():
     assert_states_equal(st.contiguous().cpu().numpy(), ref_st)
     _compare(b, out.cpu().numpy(), ref["out"])
     assert buf[0].item() == 0.0 and buf[-3:].abs().sum().item() == 0.0  # guards untouched
+
+
+@pytest.mark.parametrize("ci_stride", [2, 5])
+@pytest.mark.parametrize("state_dtype", ["f32", "bf16"])
+def test_update_strided_indices_and_decode_weight(ci_stride, state_dtype):
+    """The kda_decode page's pairing: a position-major conv state and the
+    [qkv, width, channel] weight, with cache_indices as a strided view."""
+    b = _decode_batch(540 + ci_stride, 200, 384, 128, 392, 300, col_offset=8, null_count=3,
+                      state_dtype=state_dtype)
+    st = b.conv_states.copy()
+    ref = pins.run_oracle_ex(b, states=st)
+    got, got_st = _run_update(b, True, "decode3", ci_stride)
+    assert_states_equal(got_st, st)
+    _compare(b, got, ref["out"])
+
+
+def test_update_wrapper_with_the_decode_weight():
+    """causal_conv1d_update with a bf16 position-major state and the
+    (3, 4, part_dim) weight, the layout the kda_decode page's fused decode
+    kernel takes."""
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    b = _decode_batch(550, 96, 384, 128, 384, 120, null_count=2, state_dtype="bf16")
+    dev = torch.device("cuda")
+    pm = state_to_device(np.ascontiguousarray(b.conv_states.transpose(0, 2, 1)), dev)
+    st = pm.transpose(1, 2)
+    w, _, _ = weight_to_device(b, "decode3", dev)
+    x = torch.from_numpy(b.x_buf.view(np.int16)).to(dev).view(torch.bfloat16)
+    ci = torch.from_numpy(b.cache_indices).to(dev)
+    out = pkg.causal_conv1d_update(x, st, w, torch.from_numpy(b.bias).to(dev), ci, b.part_dim,
+                                   activation="silu", null_block_id=b.null_block_id)
+    torch.cuda.synchronize()
+    ref_st = b.conv_states.copy()
+    ref = pins.run_oracle_ex(b, states=ref_st)
+    assert_states_equal(state_to_host(st.contiguous()), ref_st)
+    _compare(b, out.view(torch.int16).cpu().numpy(), ref["out"])
