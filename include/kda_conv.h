@@ -338,6 +338,34 @@ kda_status_t kda_validate_metadata(const int32_t *query_start_loc, const int32_t
                                    int64_t null_block_id, int64_t *bad_seq);
 
 /*
+ * kda_validate_metadata_device -- the checks of kda_validate_metadata on DEVICE
+ * metadata, without copying it to the host: query_start_loc (num_seqs + 1 entries)
+ * and cache_indices (num_seqs entries, cache_index_stride elements apart; 0 means
+ * 1) are device pointers. The kda_conv page leaves the metadata to the caller
+ * (packed_causal_conv1d_fn checks nothing on the device); this is the check a
+ * caller can run on the metadata it is about to pass, on the stream it will use.
+ * Two small kernels run on `stream`: the first records, for every cache line, the
+ * first sequence that uses it (an atomic minimum in a scratch array of
+ * cache_lines words) and the offset and range failures; the second marks a
+ * sequence whose line an earlier sequence holds. The library takes the scratch
+ * (cache_lines * 4 bytes + 256) with cudaMallocAsync on `stream` and returns it
+ * with cudaFreeAsync.
+ * Synchronous: the call copies the result back and synchronises `stream` before
+ * it returns, so it cannot be captured in a CUDA graph. Returns KDA_OK,
+ * KDA_ERR_METADATA with *bad_seq set exactly as kda_validate_metadata sets it
+ * (the first offending sequence in the same order of checks; num_seqs for a bad
+ * final offset), KDA_ERR_INVALID_ARG (negative sizes or stride, NULL pointers,
+ * num_seqs > 2^30, cache_lines > 2^31), or KDA_ERR_CUDA (allocation, launch or
+ * copy failure; kda_last_error_string() has CUDA's text). bad_seq may be NULL.
+ */
+kda_status_t kda_validate_metadata_device(const int32_t *query_start_loc,
+                                          const int32_t *cache_indices,
+                                          int64_t cache_index_stride, int64_t num_seqs,
+                                          int64_t tokens, int64_t cache_lines,
+                                          int64_t null_block_id, int64_t *bad_seq,
+                                          kda_stream_t stream);
+
+/*
  * kda_epilogue_range -- the device epilogue of kda_packed_conv1d on its own, for
  * checking it over all fp32 inputs. out[i] = bf16_round_nearest_even(act(f)), where
  * f is the fp32 value whose bit pattern is first + i (wrapping mod 2^32), for

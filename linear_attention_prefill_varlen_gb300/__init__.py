@@ -19,6 +19,11 @@ from ._binding import (  # noqa: F401
     KDA_DTYPE_BF16,
     KDA_DTYPE_F16,
     KDA_DTYPE_F32,
+    KDA_ERR_CUDA,
+    KDA_ERR_INVALID_ARG,
+    KDA_ERR_METADATA,
+    KDA_ERR_MISALIGNED,
+    KDA_ERR_UNSUPPORTED,
     KDA_OK,
     KdaConvLayout,
     KdaError,
@@ -42,4 +47,5 @@ from ._binding import (  # noqa: F401
     packed_causal_conv1d_fn,
     packed_causal_conv1d_supported,
     validate_metadata,
+    validate_metadata_device,
 )

@@ -1099,6 +1099,45 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
 }
 
 // ---------------------------------------------------------------------------
+// Metadata checks on the device (kda_validate_metadata_device)
+// ---------------------------------------------------------------------------
+
+// Pass 1 over the sequences: offsets that go backwards, a negative first or a
+// too-large last offset (res[0] = the smallest offending index, as the host
+// check reports it), cache indices outside [0, lines) (res[1]), and for every
+// live line the first sequence that uses it (claim[line] = the smallest s).
+// claim and res start at 0xFFFFFFFF.
+__global__ void __launch_bounds__(256) kda_validate_claim_kernel(
+    const int32_t *qsl, const int32_t *ci, int64_t ci_stride, int num_seqs, int64_t tokens,
+    int64_t lines, int64_t null_block_id, uint32_t *claim, uint32_t *res) {
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < num_seqs; s += step) {
+        const int q0 = qsl[s], q1 = qsl[s + 1];
+        if (s == 0 && q0 < 0) atomicMin(&res[0], 0u);
+        if (q1 < q0) atomicMin(&res[0], (uint32_t)s);
+        if (s == num_seqs - 1 && (int64_t)q1 > tokens) atomicMin(&res[0], (uint32_t)num_seqs);
+        const int64_t line = ci[s * ci_stride];
+        if (line == null_block_id) continue;
+        if (line < 0 || line >= lines)
+            atomicMin(&res[1], (uint32_t)s);
+        else
+            atomicMin(&claim[line], (uint32_t)s);
+    }
+}
+
+// Pass 2: a live sequence whose line an earlier sequence claimed is a duplicate.
+__global__ void __launch_bounds__(256) kda_validate_dup_kernel(
+    const int32_t *ci, int64_t ci_stride, int num_seqs, int64_t lines, int64_t null_block_id,
+    const uint32_t *claim, uint32_t *res) {
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < num_seqs; s += step) {
+        const int64_t line = ci[s * ci_stride];
+        if (line == null_block_id || line < 0 || line >= lines) continue;
+        if (claim[line] < (uint32_t)s) atomicMin(&res[1], (uint32_t)s);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -1374,6 +1413,13 @@ void dispatch(const Params &p, const Shape &sh, bool silu, cudaStream_t s) {
         dispatch_act<kDtype, true>(p, sh, silu, s);
 }
 
+// KDA_ERR_CUDA with CUDA's text for `err` (a failed runtime call).
+kda_status_t cuda_failure(cudaError_t err) {
+    snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(err),
+             cudaGetErrorString(err));
+    return KDA_ERR_CUDA;
+}
+
 kda_status_t record_cuda_error() {
     cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) err = g_launch_status;
@@ -1600,6 +1646,49 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     return record_cuda_error();
 }
 
+// The device checks with caller-provided scratch: claim (lines entries) and
+// res (2 entries), both device memory.  Enqueues on `s`, copies the two
+// results back and synchronises `s`.
+kda_status_t validate_on_device(const int32_t *qsl, const int32_t *ci, int64_t ci_stride,
+                                int64_t num_seqs, int64_t tokens, int64_t lines,
+                                int64_t null_block_id, uint32_t *claim, uint32_t *res,
+                                int64_t *bad, cudaStream_t s) {
+    cudaError_t err = cudaMemsetAsync(res, 0xFF, 2 * sizeof(uint32_t), s);
+    if (err == cudaSuccess && lines > 0)
+        err = cudaMemsetAsync(claim, 0xFF, (size_t)lines * sizeof(uint32_t), s);
+    if (err != cudaSuccess) return cuda_failure(err);
+    const int threads = 256;
+    const int64_t want = (num_seqs + threads - 1) / threads;
+    const int blocks = (int)(want < 4 * 152 ? want : 4 * 152);
+    kda_validate_claim_kernel<<<blocks, threads, 0, s>>>(qsl, ci, ci_stride, (int)num_seqs, tokens,
+                                                         lines, null_block_id, claim, res);
+    kda_validate_dup_kernel<<<blocks, threads, 0, s>>>(ci, ci_stride, (int)num_seqs, lines,
+                                                       null_block_id, claim, res);
+    kda_status_t st = record_cuda_error();
+    if (st != KDA_OK) return st;
+    uint32_t host_res[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+    err = cudaMemcpyAsync(host_res, res, sizeof host_res, cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return cuda_failure(err);
+    if (host_res[0] != 0xFFFFFFFFu) {
+        *bad = host_res[0];
+        return KDA_ERR_METADATA;
+    }
+    if (host_res[1] != 0xFFFFFFFFu) {
+        *bad = host_res[1];
+        return KDA_ERR_METADATA;
+    }
+    return KDA_OK;
+}
+
+kda_status_t check_validate_args(const int32_t *qsl, const int32_t *ci, int64_t ci_stride,
+                                 int64_t num_seqs, int64_t tokens, int64_t lines) {
+    if (num_seqs < 0 || tokens < 0 || lines < 0 || ci_stride < 0) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > (int64_t(1) << 30) || lines > (int64_t(1) << 31)) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!qsl || !ci)) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1759,6 +1848,34 @@ kda_status_t kda_validate_metadata(const int32_t *query_start_loc, const int32_t
         seen[line] = 1;
     }
     free(seen);
+    return st;
+}
+
+kda_status_t kda_validate_metadata_device(const int32_t *query_start_loc,
+                                          const int32_t *cache_indices,
+                                          int64_t cache_index_stride, int64_t num_seqs,
+                                          int64_t tokens, int64_t cache_lines,
+                                          int64_t null_block_id, int64_t *bad_seq,
+                                          kda_stream_t stream) {
+    int64_t dummy;
+    int64_t *bad = bad_seq ? bad_seq : &dummy;
+    *bad = -1;
+    kda_status_t st = check_validate_args(query_start_loc, cache_indices, cache_index_stride,
+                                          num_seqs, tokens, cache_lines);
+    if (st != KDA_OK || num_seqs == 0) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // scratch: the claim array, then the two result words (256-byte aligned)
+    const size_t claim_bytes = ((size_t)cache_lines * sizeof(uint32_t) + 255) / 256 * 256;
+    void *scratch = nullptr;
+    cudaError_t err = cudaMallocAsync(&scratch, claim_bytes + 256, s);
+    if (err != cudaSuccess) return cuda_failure(err);
+    uint32_t *claim = static_cast<uint32_t *>(scratch);
+    uint32_t *res = reinterpret_cast<uint32_t *>(static_cast<char *>(scratch) + claim_bytes);
+    st = validate_on_device(query_start_loc, cache_indices,
+                            cache_index_stride > 0 ? cache_index_stride : 1, num_seqs, tokens,
+                            cache_lines, null_block_id, claim, res, bad, s);
+    err = cudaFreeAsync(scratch, s);
+    if (st != KDA_ERR_CUDA && err != cudaSuccess) return cuda_failure(err);
     return st;
 }
 
