@@ -913,10 +913,13 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 // ---------------------------------------------------------------------------
 
 // kLayout: 0 dense weight and dense fp32 state; 1 dense weight and dense bf16
-// state; 2 any strides, width and state type (the element path); 3 (fp32
-// state) and 4 (bf16 state): the weight channel- or tap-major and the state
-// dense or position-major, every access a vector (the flags weight_tapvec /
-// state_posvec).
+// state; 2 any strides, width and state type (the element path); 3 a
+// position-major fp32 state with a channel- or tap-major weight; 4 a bf16
+// state, dense or position-major, with a channel- or tap-major weight; 5 a
+// dense fp32 state with a tap-major weight.  3, 4 and 5 move every access as
+// a vector (the flags weight_tapvec / state_posvec).  3 and 5 are separate
+// instantiations because one holding both state branches spilled at the
+// 64-register cap (24 bytes stored, 36 loaded per item).
 //
 // One (token, channel vector) of the decode update: the kernel below runs it
 // once per thread (kLayout 0, 2) or over a grid-stride loop (kLayout 1, 3, 4).
@@ -930,7 +933,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
     const int c = (int)(gid - token * nvec) * VEC;
 
     float w[VEC][4];
-    if (kLayout < 2 || p.weight_dense) {
+    if (kLayout < 2 || (kLayout != 5 && p.weight_dense)) {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
             const float4 q = __ldg(reinterpret_cast<const float4 *>(p.weight) + (c + v));
@@ -982,7 +985,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
     const int64_t line = __ldg(p.cache_indices + token * p.ci_stride);
     const bool live = line != p.null_block_id;
     float h0[VEC], h1[VEC], h2[VEC];
-    if (kLayout < 2 || p.state_dense) {
+    if (kLayout < 2 || kLayout == 5 || (kLayout != 3 && p.state_dense)) {
         const bool bf16 = kLayout == 1 || kLayout == 4 || (kLayout == 2 && p.state_bf16);
         void *sp = state_line_ptr(p, line, c, bf16);
         float st[3 * VEC];
@@ -1006,7 +1009,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
             }
             store_state3<VEC>(sp, bf16, ns);
         }
-    } else if (kLayout >= 3) {
+    } else if (kLayout == 3 || kLayout == 4) {
         // Position-major: position k of channels c .. c+3 is one vector at
         // base + k * s2.  Read positions K-3 .. K-1; then move positions
         // 1 .. K-1 down by one (K-3 of them from registers) and write x at K-1.
@@ -1586,8 +1589,12 @@ void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s)
             dispatch_update_act<kDtype, 4>(
                 p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
                 s);
-        else
+        else if (p.state_posvec)
             dispatch_update_act<kDtype, 3>(
+                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
+                s);
+        else  // a dense fp32 state: the weight is tap-major (both dense is layout 0)
+            dispatch_update_act<kDtype, 5>(
                 p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
                 s);
     else
