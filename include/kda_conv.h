@@ -366,6 +366,34 @@ kda_status_t kda_validate_metadata_device(const int32_t *query_start_loc,
                                           kda_stream_t stream);
 
 /*
+ * kda_validate_metadata_device_noalloc -- kda_validate_metadata_device for callers
+ * that cannot allocate device memory. The pages have no counterpart: this entry
+ * point exists for callers such as a serving engine that has reserved all of the
+ * GPU's memory up front for its own pool (so a cudaMalloc or cudaMallocAsync of
+ * its own would fail or take memory the engine has promised elsewhere), or a
+ * host thread that must not make the driver calls, and their possible
+ * synchronisation, that allocating and freeing involve.
+ * Same arguments, checks, results and synchronisation as
+ * kda_validate_metadata_device, but the scratch is a fixed array inside the
+ * library, 1 MiB of device memory on every GPU that loads the library, held until
+ * the process exits: cache_lines may be at most 262144 (2^18); a larger value
+ * returns KDA_ERR_UNSUPPORTED (kda_last_error_string() says why) before any CUDA
+ * call. The call allocates nothing and frees nothing. The first call on a device
+ * looks up that array's device address (cudaGetSymbolAddress, with that device
+ * current) and keeps it; make that first call before any stream capture begins.
+ * Every call shares the one array: the call clears the words it uses before its
+ * kernels run, so an earlier call's leftovers do not matter, but two calls whose
+ * work overlaps on the GPU (other streams, other host threads, the same device)
+ * race on it and may both report wrong results. Serialise them.
+ */
+kda_status_t kda_validate_metadata_device_noalloc(const int32_t *query_start_loc,
+                                                  const int32_t *cache_indices,
+                                                  int64_t cache_index_stride, int64_t num_seqs,
+                                                  int64_t tokens, int64_t cache_lines,
+                                                  int64_t null_block_id, int64_t *bad_seq,
+                                                  kda_stream_t stream);
+
+/*
  * kda_epilogue_range -- the device epilogue of kda_packed_conv1d on its own, for
  * checking it over all fp32 inputs. out[i] = bf16_round_nearest_even(act(f)), where
  * f is the fp32 value whose bit pattern is first + i (wrapping mod 2^32), for

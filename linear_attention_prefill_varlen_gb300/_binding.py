@@ -94,6 +94,8 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
     handle.kda_validate_metadata.argtypes = [P, P, I64, I64, I64, I64, ctypes.POINTER(I64)]
     handle.kda_validate_metadata_device.argtypes = [P, P, I64, I64, I64, I64, I64,
                                                     ctypes.POINTER(I64), P]
+    handle.kda_validate_metadata_device_noalloc.argtypes = [P, P, I64, I64, I64, I64, I64,
+                                                            ctypes.POINTER(I64), P]
     handle.kda_epilogue_range.argtypes = [ctypes.c_uint32, ctypes.c_uint64, C, P, P]
     for name in ("kda_packed_conv1d", "kda_packed_conv1d_preact_f32", "kda_packed_conv1d_ex",
                  "kda_conv1d_update", "kda_packed_conv1d_l2norm", "kda_conv1d_update_l2norm",
@@ -101,7 +103,7 @@ def _declare(handle: ctypes.CDLL) -> ctypes.CDLL:
                  "kda_packed_conv1d_ex_check_args",
                  "kda_packed_conv1d_check_args", "kda_packed_conv1d_launch_shape",
                  "kda_validate_metadata", "kda_validate_metadata_device",
-                 "kda_epilogue_range"):
+                 "kda_validate_metadata_device_noalloc", "kda_epilogue_range"):
         getattr(handle, name).restype = C
     handle.kda_status_string.argtypes = [C]
     handle.kda_status_string.restype = ctypes.c_char_p
@@ -303,10 +305,13 @@ def validate_metadata(query_start_loc, cache_indices, tokens: int, cache_lines: 
 
 def validate_metadata_device(query_start_loc: torch.Tensor, cache_indices: torch.Tensor,
                              tokens: int, cache_lines: int, null_block_id: int,
-                             stream=None) -> tuple[int, int]:
+                             stream=None, noalloc: bool = False) -> tuple[int, int]:
     """C-ABI kda_validate_metadata_device on CUDA int32 tensors (cache_indices
     may be a strided 1-D view), without copying them to the host; synchronises
-    the stream.  Returns (status, bad seq) as validate_metadata does."""
+    the stream.  Returns (status, bad seq) as validate_metadata does.
+    noalloc=True calls kda_validate_metadata_device_noalloc instead: the same
+    check on the library's fixed device scratch, for a caller that cannot
+    allocate (at most 262144 cache lines; calls must not overlap)."""
     for name, t in (("query_start_loc", query_start_loc), ("cache_indices", cache_indices)):
         if t.dtype != torch.int32 or t.dim() != 1 or not t.is_cuda:
             raise ValueError(f"{name} must be a 1-D CUDA int32 tensor")
@@ -317,9 +322,10 @@ def validate_metadata_device(query_start_loc: torch.Tensor, cache_indices: torch
         raise ValueError(f"cache_indices has {cache_indices.numel()} entries, {num_seqs} needed")
     stride = cache_indices.stride(0) if cache_indices.numel() > 1 else 1
     bad = ctypes.c_int64(-1)
-    st = lib().kda_validate_metadata_device(
-        query_start_loc.data_ptr(), cache_indices.data_ptr(), stride, num_seqs, tokens,
-        cache_lines, null_block_id, ctypes.byref(bad), _stream(stream))
+    fn = (lib().kda_validate_metadata_device_noalloc if noalloc
+          else lib().kda_validate_metadata_device)
+    st = fn(query_start_loc.data_ptr(), cache_indices.data_ptr(), stride, num_seqs, tokens,
+            cache_lines, null_block_id, ctypes.byref(bad), _stream(stream))
     if st == KDA_ERR_CUDA:
         _check(st)
     return st, bad.value

@@ -1140,6 +1140,13 @@ __global__ void __launch_bounds__(256) kda_validate_dup_kernel(
     }
 }
 
+// Scratch for kda_validate_metadata_device_noalloc: the claim array of up to
+// kNoAllocLines cache lines, then the two result words.  Every GPU that loads
+// the library holds it (1 MiB) until the process exits; every call of that
+// entry point shares it.
+constexpr int64_t kNoAllocLines = int64_t(1) << 18;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocLines + 64];
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1688,6 +1695,30 @@ kda_status_t validate_on_device(const int32_t *qsl, const int32_t *ci, int64_t c
     return KDA_OK;
 }
 
+// The device address of g_noalloc_scratch on the current device, looked up
+// once per device with that device current (in host code the symbol's name
+// is a host-side stand-in, not a device address).  Returns nullptr and sets
+// *err if the lookup fails.
+uint32_t *noalloc_scratch(cudaError_t *err) {
+    static std::atomic<uint32_t *> cache[64];
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= 64) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    uint32_t *ptr = cache[dev].load(std::memory_order_acquire);
+    if (ptr == nullptr) {
+        void *addr = nullptr;
+        *err = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+        if (*err != cudaSuccess) return nullptr;
+        ptr = static_cast<uint32_t *>(addr);
+        cache[dev].store(ptr, std::memory_order_release);  // racing threads store the same value
+    }
+    return ptr;
+}
+
 kda_status_t check_validate_args(const int32_t *qsl, const int32_t *ci, int64_t ci_stride,
                                  int64_t num_seqs, int64_t tokens, int64_t lines) {
     if (num_seqs < 0 || tokens < 0 || lines < 0 || ci_stride < 0) return KDA_ERR_INVALID_ARG;
@@ -1884,6 +1915,35 @@ kda_status_t kda_validate_metadata_device(const int32_t *query_start_loc,
     err = cudaFreeAsync(scratch, s);
     if (st != KDA_ERR_CUDA && err != cudaSuccess) return cuda_failure(err);
     return st;
+}
+
+kda_status_t kda_validate_metadata_device_noalloc(const int32_t *query_start_loc,
+                                                  const int32_t *cache_indices,
+                                                  int64_t cache_index_stride, int64_t num_seqs,
+                                                  int64_t tokens, int64_t cache_lines,
+                                                  int64_t null_block_id, int64_t *bad_seq,
+                                                  kda_stream_t stream) {
+    int64_t dummy;
+    int64_t *bad = bad_seq ? bad_seq : &dummy;
+    *bad = -1;
+    kda_status_t st = check_validate_args(query_start_loc, cache_indices, cache_index_stride,
+                                          num_seqs, tokens, cache_lines);
+    if (st != KDA_OK || num_seqs == 0) return st;
+    if (cache_lines > kNoAllocLines) {
+        snprintf(g_last_error, sizeof g_last_error,
+                 "cache_lines %lld exceeds the %lld lines of the static scratch",
+                 (long long)cache_lines, (long long)kNoAllocLines);
+        return KDA_ERR_UNSUPPORTED;
+    }
+    cudaError_t err = cudaSuccess;
+    uint32_t *scratch = noalloc_scratch(&err);
+    if (scratch == nullptr) return cuda_failure(err);
+    // validate_on_device clears the claim words it uses and the two result
+    // words before its kernels run, whatever an earlier call left there.
+    return validate_on_device(query_start_loc, cache_indices,
+                              cache_index_stride > 0 ? cache_index_stride : 1, num_seqs, tokens,
+                              cache_lines, null_block_id, scratch, scratch + kNoAllocLines, bad,
+                              static_cast<cudaStream_t>(stream));
 }
 
 kda_status_t kda_epilogue_range(uint32_t first, uint64_t count, int activation, uint16_t *out,
