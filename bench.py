@@ -391,6 +391,51 @@ def settle(dev, stream, seconds: float = SETTLE_S) -> None:
     del a, c
 
 
+def prepare(pkg, b: workloads.Batch, s: dict, stream: int):
+    """The C function and argument tuple of the call `call` makes on set s,
+    every pointer and struct reference converted beforehand, so that a timed
+    step is the C-ABI call alone.  Returns (function, args)."""
+    import ctypes
+
+    lib = pkg.lib()
+    if "layout" not in s:
+        s["layout"] = state_layout(pkg, b, s)
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    def ref(o):
+        return None if o is None else ctypes.byref(o)
+
+    common = (s["x_ptr"], s["x_row_stride"], b.tokens, b.dim, b.part_dim, ptr(s["weight"]),
+              ptr(s["bias"]), ptr(s["conv_states"]), ptr(s["cache_indices"]))
+    packed_meta = (ptr(s["has_initial_state"]), ptr(s["query_start_loc"]), b.num_seqs)
+    lay = s["layout"]
+    if NORM is not None:
+        if lay is None and ENTRY == "update":
+            lay = s["norm_layout"] = pkg.make_layout(pkg.KDA_DTYPE_BF16, 3, (3 * b.dim, 3, 1),
+                                                     (4, 1))
+        if ENTRY == "update":
+            return lib.kda_conv1d_update_l2norm, common + (
+                b.null_block_id, b.activation, ptr(s["out"]), ref(lay), ref(NORM), stream)
+        return lib.kda_packed_conv1d_l2norm, common + packed_meta + (
+            b.null_block_id, b.activation, ptr(s["out"]), ref(lay), ref(NORM), stream)
+    if ENTRY == "update":
+        return lib.kda_conv1d_update, common + (b.null_block_id, b.activation, ptr(s["out"]),
+                                                ref(lay), stream)
+    if lay is not None:
+        return lib.kda_packed_conv1d_ex, common + packed_meta + (
+            b.null_block_id, b.activation, ptr(s["out"]), ref(lay), stream)
+    return lib.kda_packed_conv1d, common + packed_meta + (b.null_block_id, b.activation,
+                                                          ptr(s["out"]), stream)
+
+
+def check_statuses(pkg, statuses) -> None:
+    bad = [st for st in statuses if st != 0]
+    if bad:
+        pkg._binding._check(bad[0])
+
+
 def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, dist: Dist,
                 dev, flush: torch.Tensor | None = None) -> dict:
     """W untimed steps, then exactly K timed steps between barrier+sync pairs,
@@ -419,21 +464,25 @@ def time_device(pkg, b: workloads.Batch, sets: list, steps: int, warmup: int, di
         settle(dev, stream)
         for i in range(warmup):
             call(pkg, b, sets[i % len(sets)], stream.cuda_stream)
+        # the rotation continues from the warm-up: no step reuses the set of
+        # the step before it; each step is the prepared C-ABI call
+        prepared = [prepare(pkg, b, sets[(warmup + i) % len(sets)], stream.cuda_stream)
+                    for i in range(steps)]
+        statuses = []
         dist.barrier()
         torch.cuda.synchronize(dev)
         region0.record(stream)
-        for i in range(steps):
+        for i, (fn, args) in enumerate(prepared):
             if flush is not None:
                 with torch.cuda.stream(stream):
                     flush.fill_(i & 0xFF)
                 starts[i].record(stream)
-            # the rotation continues from the warm-up: no step reuses the set
-            # of the step before it
-            call(pkg, b, sets[(warmup + i) % len(sets)], stream.cuda_stream)
+            statuses.append(fn(*args))
             if flush is not None:
                 ends[i].record(stream)
         region1.record(stream)
         torch.cuda.synchronize(dev)
+        check_statuses(pkg, statuses)
     dist.barrier()
     region_ms = region0.elapsed_time(region1)
     if flush is not None:
