@@ -63,3 +63,43 @@ def test_our_arm_fails_loudly_without_a_gpu():
     assert r.returncode != 0
     assert r.stdout.strip() == ""  # no number printed
     assert "GPU" in r.stderr
+
+
+@pytest.mark.parametrize("entry,norm,layout", [
+    ("packed", False, ("dense", "channel_major")),
+    ("packed", False, ("position_major", "tap_major")),
+    ("packed", True, ("dense", "channel_major")),
+    ("packed", True, ("position_major", "channel_major")),
+    ("update", False, ("dense", "channel_major")),
+    ("update", False, ("position_major", "tap_major")),
+    ("update", True, ("dense", "channel_major")),
+])
+def test_prepared_step_matches_the_c_signature(entry, norm, layout):
+    """The timed step's prepared C call (bench.prepare) passes exactly the
+    arguments its C function declares, for every entry point the bench can
+    time.  Host tensors stand in for device ones: nothing is called."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads
+    import linear_attention_prefill_varlen_gb300 as pkg
+
+    old = (bench.ENTRY, bench.NORM, dict(bench.LAYOUT_OPTS))
+    try:
+        bench.ENTRY = entry
+        bench.NORM = pkg.make_l2norm(0b011, 64, 1e-6) if norm else None
+        bench.LAYOUT_OPTS.update(state_layout=layout[0], weight_layout=layout[1])
+        b = workloads.make_batch("prep", 3, [1] * 4 if entry == "update" else [3, 5],
+                                 256, 128, 264, 8)
+        s = bench.upload(b, torch.device("cpu"))
+        fn, args = bench.prepare(pkg, b, s, 0)
+        assert len(args) == len(fn.argtypes), (fn.__name__, len(args), len(fn.argtypes))
+        want = {("packed", False): "kda_packed_conv1d", ("update", False): "kda_conv1d_update",
+                ("packed", True): "kda_packed_conv1d_l2norm",
+                ("update", True): "kda_conv1d_update_l2norm"}[(entry, norm)]
+        if entry == "packed" and not norm and layout != ("dense", "channel_major"):
+            want = "kda_packed_conv1d_ex"
+        assert fn.__name__ == want
+    finally:
+        bench.ENTRY, bench.NORM = old[0], old[1]
+        bench.LAYOUT_OPTS.clear()
+        bench.LAYOUT_OPTS.update(old[2])
