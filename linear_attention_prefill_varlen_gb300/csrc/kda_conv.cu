@@ -90,6 +90,31 @@ namespace {
 
 constexpr int kMaxStateWidth = 64;
 
+// Division by a divisor fixed for a launch, as a multiply-high and two
+// shifts (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): for 1 <= d < 2^31, l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, every n < 2^32 has
+// n / d = (t + ((n - t) >> min(l, 1))) >> max(l - 1, 0), t = umulhi(m, n).
+struct FastDiv {
+    uint32_t m;
+    int s1, s2;
+};
+
+FastDiv make_fast_div(uint32_t d) {
+    int l = 0;
+    while ((uint64_t(1) << l) < d) ++l;
+    FastDiv f;
+    f.m = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+    f.s1 = l < 1 ? l : 1;
+    f.s2 = l > 1 ? l - 1 : 0;
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+    const uint32_t t = __umulhi(f.m, n);
+    return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 struct Params {
     const void *x;
     int64_t x_row_stride;  // elements
@@ -122,6 +147,8 @@ struct Params {
     int64_t plane_stride;  // tokens * part_dim elements
     int chunk;             // tokens per program (>= 4)
     int warps_per_prog;    // warps covering one program's channel vectors
+    FastDiv chunk_div;     // division by chunk
+    FastDiv wpp_div;       // division by warps_per_prog
     int64_t total_warps;   // programs * warps_per_prog
     int search_steps;      // radix-32 levels: smallest s with 32^s >= num_seqs
     int search_top;        // 32^(search_steps - 1)
@@ -520,7 +547,7 @@ __device__ __forceinline__ int find_sequence(const Params &p, int prog, int lane
     for (int level = 0; level < p.search_steps; ++level) {
         const int idx = base + lane * stride;
         bool ok = false;
-        if (idx < p.num_seqs) ok = (__ldg(p.qsl + idx) / p.chunk + idx) <= prog;
+        if (idx < p.num_seqs) ok = (int)fast_div((uint32_t)__ldg(p.qsl + idx), p.chunk_div) + idx <= prog;
         const unsigned m = __ballot_sync(0xFFFFFFFFu, ok);
         if (m == 0u) return -1;
         base += (__popc(m) - 1) * stride;
@@ -631,7 +658,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
     const int lane = threadIdx.x & 31;
     const int64_t gwarp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (gwarp >= p.total_warps) return;  // whole warps only
-    const int prog = (int)(gwarp / p.warps_per_prog);
+    const int prog = (int)fast_div((uint32_t)gwarp, p.wpp_div);  // total_warps < 2^32
     const int wv = (int)(gwarp - (int64_t)prog * p.warps_per_prog);
 
     int s, q0, q1;
@@ -644,13 +671,15 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
         q0 = __ldg(p.qsl + s);
         q1 = __ldg(p.qsl + s + 1);
     }
-    const int f_s = q0 / p.chunk + s;
+    // A negative offset (malformed metadata) divides as a huge one: the
+    // program is then idle, and nothing outside x and out is touched.
+    const int64_t f_s = (int64_t)fast_div((uint32_t)q0, p.chunk_div) + s;
     if (f_s > prog) return;
     // Clamp the sequence to [0, tokens) so that malformed offsets never read or
     // write outside x / out.
     const int a = max(q0, 0);
     const int e = min(q1, p.tokens);
-    const int k = prog - f_s;
+    const int k = (int)(prog - f_s);
     const int64_t t0_wide = (int64_t)a + (int64_t)k * p.chunk;
     if (t0_wide >= e) return;
     const int t0 = (int)t0_wide;
@@ -1557,7 +1586,8 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
         (l.x_dtype == KDA_DTYPE_F32 ? min_blocks<KDA_DTYPE_F32>() : min_blocks<KDA_DTYPE_BF16>()) -
         (norm_on ? 2 : 0);
     const Shape sh = launch_shape(tokens, dim, num_seqs, current_sms(), blocks_per_sm);
-    if (sh.ctas > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    // warp and program indices are divided in 32 bits on the device
+    if (sh.ctas > INT32_MAX || sh.total_warps >= (int64_t(1) << 32)) return KDA_ERR_INVALID_ARG;
     Params p;
     p.x = x;
     p.x_row_stride = x_row_stride;
@@ -1587,6 +1617,8 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.plane_stride = tokens * part_dim;
     p.chunk = sh.chunk;
     p.warps_per_prog = sh.warps_per_prog;
+    p.chunk_div = make_fast_div((uint32_t)sh.chunk);
+    p.wpp_div = make_fast_div((uint32_t)sh.warps_per_prog);
     p.total_warps = sh.total_warps;
     int steps = 0;
     int64_t reach = 1;

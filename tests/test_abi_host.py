@@ -381,3 +381,29 @@ def test_chunk_bounded_for_many_sequences(kda):
     # small batches keep the one-wave fit (no less than 48 rows from the cap)
     assert kda.launch_shape(2430, 4608, 1536, 8)["chunk"] == 24
     assert kda.launch_shape(2600, 4608, 1536, 31)["chunk"] == 30
+
+
+def test_fast_division_model():
+    """Host model of the kernel's division by a launch-fixed divisor (chunk,
+    warps per program): with l = ceil(log2 d), m = floor(2^32 (2^l - d) / d)
+    + 1, t = umulhi(m, n), the quotient (t + ((n - t) >> min(l, 1))) >>
+    max(l - 1, 0) equals n // d for every 32-bit n, checked for d = 1..4096,
+    powers of two and their neighbours up to 2^30, and random d, against
+    edge and random numerators."""
+    rng = np.random.default_rng(17)
+    ds = list(range(1, 4097)) + [2 ** k + o for k in range(12, 31) for o in (-1, 0, 1)]
+    ds += [int(v) for v in rng.integers(1, 2 ** 31, size=300)]
+    for d in ds:
+        l = 0
+        while (1 << l) < d:
+            l += 1
+        m = ((1 << 32) * ((1 << l) - d)) // d + 1
+        assert 0 < m < (1 << 32)
+        s1, s2 = min(l, 1), max(l - 1, 0)
+        n = np.concatenate([np.array([0, 1, d - 1, d, d + 1, 2 * d - 1, 2 * d, 2 ** 32 - 1,
+                                      2 ** 31, (2 ** 32 - 1) // d * d], dtype=np.uint64),
+                            rng.integers(0, 2 ** 32, size=200, dtype=np.uint64)])
+        n = n[n < 2 ** 32]
+        t = (np.uint64(m) * n) >> np.uint64(32)
+        q = (t + ((n - t) >> np.uint64(s1))) >> np.uint64(s2)
+        assert np.array_equal(q, n // np.uint64(d)), d
