@@ -150,7 +150,9 @@ typedef struct kda_conv_layout {
  * num_seqs >= 0.
  *
  * Returns KDA_OK after enqueueing the launch on `stream` (or without a launch when
- * tokens == 0 or num_seqs == 0). Argument errors return without touching memory.
+ * tokens == 0 or num_seqs == 0). Argument errors return without touching memory;
+ * sizes whose launch would need 2^32 warps or more (program and warp indices are
+ * divided in 32 bits on the device) return KDA_ERR_INVALID_ARG.
  * The metadata (query_start_loc, cache_indices) is the caller's contract and is
  * not checked on the device beyond clamping token rows to [0, tokens): a cache
  * index outside [0, cache_lines) other than null_block_id, or two live sequences
@@ -202,8 +204,9 @@ kda_status_t kda_packed_conv1d_ex(const void *x, int64_t x_row_stride, int64_t t
  * whose base is 16-byte (fp32) or 8-byte (bf16) aligned. The other is a
  * tap-major weight (strides (1, a multiple of 4), 16-byte aligned). Other
  * strides are read and written element by element. Cache indices must
- * be distinct (or null); out must not overlap x or conv_states. Asynchronous on
- * `stream`; allocates nothing.
+ * be distinct (or null); out must not overlap x or conv_states. batch * dim / 4
+ * must be below 2^32 (KDA_ERR_INVALID_ARG otherwise). Asynchronous on `stream`;
+ * allocates nothing.
  */
 kda_status_t kda_conv1d_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
                               int64_t part_dim, const float *weight, const float *bias,

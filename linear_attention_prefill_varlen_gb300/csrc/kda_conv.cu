@@ -149,6 +149,8 @@ struct Params {
     int warps_per_prog;    // warps covering one program's channel vectors
     FastDiv chunk_div;     // division by chunk
     FastDiv wpp_div;       // division by warps_per_prog
+    FastDiv part_div;      // division by part_dim
+    FastDiv nvec_div;      // division by dim / VEC (the decode update's item index)
     int64_t total_warps;   // programs * warps_per_prog
     int search_steps;      // radix-32 levels: smallest s with 32^s >= num_seqs
     int search_top;        // 32^(search_steps - 1)
@@ -366,7 +368,7 @@ __device__ __forceinline__ void state_set4(const Params &p, int64_t i, bool bf16
 // Element offset of weight[c][0] (c's part, then c within the part).  A
 // thread's VEC channels never straddle a part (part_dim % 64 == 0, c % VEC == 0).
 __device__ __forceinline__ int64_t weight_base(const Params &p, int c) {
-    const int part = c / p.part_dim;
+    const int part = (int)fast_div((uint32_t)c, p.part_div);
     return (int64_t)part * p.w_stride_part + (int64_t)(c - part * p.part_dim) * p.w_stride_c;
 }
 
@@ -758,7 +760,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
             float y[VEC];
             taps_row<VEC, kBias>(w, bias, g0, g1, g2, xv, y);
             if constexpr (kSilu) silu_row<VEC>(y);
-            const int plane1 = c / p.part_dim;
+            const int plane1 = (int)fast_div((uint32_t)c, p.part_div);
             if constexpr (kNorm) {
                 if ((p.norm_mask >> plane1) & 1u)
                     l2norm_row<VEC>(y, p.norm_eps, p.norm_lanes, head_group_mask(lane, p.norm_lanes));
@@ -872,7 +874,7 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
         widen<VEC, kDtype>(raw, h2);
     }
 
-    const int plane = c / p.part_dim;
+    const int plane = (int)fast_div((uint32_t)c, p.part_div);
     const int col = c - plane * p.part_dim;
     const int64_t out_row = p.part_dim;  // elements between output rows
     // Heads never straddle planes, so a head group agrees on norm_on.
@@ -1026,7 +1028,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
     constexpr int W = row_words<VEC, kDtype>();
     using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
     const int64_t nvec = p.dim / VEC;
-    const int64_t token = gid / nvec;
+    const int64_t token = fast_div((uint32_t)gid, p.nvec_div);  // items < 2^32
     if (token >= p.tokens) return;
     const int c = (int)(gid - token * nvec) * VEC;
 
@@ -1161,7 +1163,7 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
     float y[VEC];
     taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);  // the history is not used after
     if constexpr (kSilu) silu_row<VEC>(y);
-    const int plane = c / p.part_dim;
+    const int plane = (int)fast_div((uint32_t)c, p.part_div);
     if constexpr (kNorm) {
         // A head group is `norm_lanes` consecutive threads of one token (dim is
         // a multiple of head_dim), so the group exits or stays together above.
@@ -1619,6 +1621,7 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.warps_per_prog = sh.warps_per_prog;
     p.chunk_div = make_fast_div((uint32_t)sh.chunk);
     p.wpp_div = make_fast_div((uint32_t)sh.warps_per_prog);
+    p.part_div = make_fast_div((uint32_t)part_dim);
     p.total_warps = sh.total_warps;
     int steps = 0;
     int64_t reach = 1;
@@ -1723,7 +1726,8 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     if (batch == 0 || dim == 0) return KDA_OK;
     const int64_t threads_total = batch * (dim / kVec);
     const int64_t blocks = (threads_total + 255) / 256;
-    if (blocks > INT32_MAX) return KDA_ERR_INVALID_ARG;
+    // item indices are divided in 32 bits on the device
+    if (blocks > INT32_MAX || threads_total >= (int64_t(1) << 32)) return KDA_ERR_INVALID_ARG;
     Params p{};
     p.x = x;
     p.x_row_stride = x_row_stride;
@@ -1749,6 +1753,8 @@ kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int6
     p.null_block_id = null_block_id;
     p.out = out;
     p.plane_stride = batch * part_dim;
+    p.part_div = make_fast_div((uint32_t)part_dim);
+    p.nvec_div = make_fast_div((uint32_t)(dim / kVec));
     set_norm(p, norm);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool silu = activation == KDA_ACT_SILU;

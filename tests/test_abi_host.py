@@ -407,3 +407,17 @@ def test_fast_division_model():
         t = (np.uint64(m) * n) >> np.uint64(32)
         q = (t + ((n - t) >> np.uint64(s1))) >> np.uint64(s2)
         assert np.array_equal(q, n // np.uint64(d)), d
+
+
+def test_index_range_limits(kda):
+    """Launch sizes whose device-side 32-bit index division would overflow
+    are rejected before any CUDA call: a decode update of 2^34 (token,
+    vector) items, and a packed launch of more than 2^32 warps."""
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_conv1d_update(A16, 4096, 1 << 24, 4096, 1024, A16, A16, A16, A16, -1, 1, A16,
+                              None, stream=0)
+    assert e.value.status == kda.KDA_ERR_INVALID_ARG
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_packed_conv1d(A16, 1 << 24, (1 << 31) - 1, 1 << 24, 1 << 22, A16, A16, A16, A16,
+                              A16, A16, 1, -1, 1, A16, stream=0)
+    assert e.value.status == kda.KDA_ERR_INVALID_ARG
