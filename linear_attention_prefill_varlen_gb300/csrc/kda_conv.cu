@@ -1023,16 +1023,10 @@ __global__ void __launch_bounds__(256) kda_epilogue_range_kernel(uint32_t first,
 //
 // One (token, channel vector) of the decode update: the kernel below runs it
 // once per thread (kLayout 0, 2) or over a grid-stride loop (kLayout 1, 3, 4).
-template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
-__device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
-    constexpr int W = row_words<VEC, kDtype>();
-    using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
-    const int64_t nvec = p.dim / VEC;
-    const int64_t token = fast_div((uint32_t)gid, p.nvec_div);  // items < 2^32
-    if (token >= p.tokens) return;
-    const int c = (int)(gid - token * nvec) * VEC;
-
-    float w[VEC][4];
+// The taps and bias of channels c .. c+VEC-1.
+template <int VEC, int kLayout, bool kBias>
+__device__ __forceinline__ void update_weights(const Params &p, int c, float (&w)[VEC][4],
+                                               float (&bias)[VEC]) {
     if (kLayout < 2 || (kLayout != 5 && p.weight_dense)) {
 #pragma unroll
         for (int v = 0; v < VEC; ++v) {
@@ -1066,7 +1060,6 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
                 w[v][j] = __ldg(p.weight + wb + v * p.w_stride_c + j * p.w_stride_j);
         }
     }
-    float bias[VEC];
 #pragma unroll
     for (int i = 0; i < VEC / 4; ++i) {
         float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1076,7 +1069,14 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
         bias[4 * i + 2] = q.z;
         bias[4 * i + 3] = q.w;
     }
+}
 
+// Token `token` of channels c .. c+VEC-1, given their taps and bias.
+template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
+__device__ __forceinline__ void update_token(const Params &p, int64_t token, int c,
+                                             const float (&w)[VEC][4], const float (&bias)[VEC]) {
+    constexpr int W = row_words<VEC, kDtype>();
+    using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
     uint32_t raw[W];
     load_row<W>(static_cast<const XT *>(p.x) + token * p.x_row_stride + c, raw);
     float xv[VEC];
@@ -1176,6 +1176,25 @@ __device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
         static_cast<XT *>(p.out) + (int64_t)plane * p.plane_stride + token * p.part_dim + col, y);
 }
 
+// One (token, channel vector) item, gid = token * (dim / VEC) + vector.
+template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
+__device__ __forceinline__ void update_item(const Params &p, int64_t gid) {
+    const int64_t nvec = p.dim / VEC;
+    const int64_t token = fast_div((uint32_t)gid, p.nvec_div);  // items < 2^32
+    if (token >= p.tokens) return;
+    const int c = (int)(gid - token * nvec) * VEC;
+    float w[VEC][4], bias[VEC];
+    update_weights<VEC, kLayout, kBias>(p, c, w, bias);
+    update_token<VEC, kDtype, kLayout, kSilu, kBias, kNorm>(p, token, c, w, bias);
+}
+
+// The layouts whose kernel keeps a channel vector per thread and loops over
+// the tokens on a 2-D grid (the others take one item per thread, or a flat
+// grid looping over the items).
+__host__ __device__ constexpr bool token_loop_layout(int layout, bool norm) {
+    return layout == 1 || layout == 5 || (!norm && (layout == 3 || layout == 4));
+}
+
 template <int VEC, int kDtype, int kLayout, bool kSilu, bool kBias, bool kNorm>
 __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     kda_conv1d_update_kernel(const Params p) {
@@ -1183,20 +1202,35 @@ __global__ void __launch_bounds__(256, kLayout == 2 ? 2 : 4)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" :::);
 #endif
-    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if constexpr (kLayout == 1 || kLayout >= 3) {
-        // A grid of (resident CTAs per SM) x SMs looping over the items: for
-        // the bf16-state and vector-layout steps it beats one thread per item
-        // (GB300, 1024 x 4608: bf16 dense 16.4 against 17.5 us, bf16
-        // position-major 18.9 against 20.1 us, fp32 position-major 26.5
-        // against 29.7 us); for the fp32 dense step it did not (23.3 against
-        // 23.0 us).  Lanes advance together, so head groups stay whole for
-        // the L2 norm.
+    constexpr bool kTokenLoop = token_loop_layout(kLayout, kNorm);
+    if constexpr (kTokenLoop) {
+        // A grid of about (resident CTAs per SM) x SMs whose threads keep one
+        // channel vector (blockIdx.x, threadIdx.x) and loop over the tokens
+        // (blockIdx.y, step gridDim.y): the taps and bias are loaded once per
+        // thread.  GB300, 1024 x 4608, against a grid-stride loop over the
+        // items that reloads them: bf16 dense state 16.3 -> 15.8 us (17.0 ->
+        // 16.7 us with the norm), bf16 position-major 19.1 -> 18.7 us, a dense
+        // fp32 state with a tap-major weight 24.4 -> 23.7 us (24.1 -> 23.6 us
+        // with the norm); the fp32 position-major state with a channel-major
+        // weight 25.0 -> 25.3 us.
+        const int v = blockIdx.x * blockDim.x + threadIdx.x;
+        if (v >= p.dim / VEC) return;
+        const int c = v * VEC;
+        float w[VEC][4], bias[VEC];
+        update_weights<VEC, kLayout, kBias>(p, c, w, bias);
+        for (int64_t token = blockIdx.y; token < p.tokens; token += gridDim.y)
+            update_token<VEC, kDtype, kLayout, kSilu, kBias, kNorm>(p, token, c, w, bias);
+    } else if constexpr (kLayout == 1 || kLayout >= 3) {
+        // With the L2 norm the taps held across the loop made the
+        // position-major variants spill or slow down (fp32: 25.8 -> 27.3 us),
+        // so these keep a grid of (resident CTAs per SM) x SMs looping over
+        // the items.  Lanes advance together, so head groups stay whole.
         const int64_t total = (int64_t)p.tokens * (p.dim / VEC);
         const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-        for (int64_t g = gid; g < total; g += stride)
+        for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += stride)
             update_item<VEC, kDtype, kLayout, kSilu, kBias, kNorm>(p, g);
     } else {
+        const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
         update_item<VEC, kDtype, kLayout, kSilu, kBias, kNorm>(p, gid);
     }
 }
@@ -1458,11 +1492,11 @@ int current_sms() {
 // that of a plain launch; what overlaps is the launch and the block
 // scheduling, not any memory access.  After any other kind of predecessor
 // the launch behaves as a plain one.
-void launch_kernel(void (*kernel)(Params), unsigned blocks, unsigned threads, const Params &p,
+void launch_kernel(void (*kernel)(Params), dim3 blocks, unsigned threads, const Params &p,
                    cudaStream_t stream) {
 #if KDA_PDL
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks);
+    cfg.gridDim = blocks;
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -1482,11 +1516,11 @@ void launch_norm(const Params &p, const Shape &sh, cudaStream_t stream) {
     if (sh.short_seqs)
         launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu,
                                                kBias, true, kNorm>,
-                      (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+                      dim3((unsigned)sh.ctas), (unsigned)sh.threads, p, stream);
     else
         launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu,
                                                kBias, false, kNorm>,
-                      (unsigned)sh.ctas, (unsigned)sh.threads, p, stream);
+                      dim3((unsigned)sh.ctas), (unsigned)sh.threads, p, stream);
 }
 
 template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
@@ -1659,57 +1693,63 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     return record_cuda_error();
 }
 
+// blocks: the grid of the layout's token loop (or one item per thread);
+// norm_blocks: the flat grid the norm variant takes where it has no token loop.
 template <int kDtype, int kLayout, bool kSilu, bool kBias>
-void launch_update(const Params &p, int64_t blocks, cudaStream_t stream) {
+void launch_update(const Params &p, dim3 blocks, dim3 norm_blocks, cudaStream_t stream) {
     if (p.norm_mask != 0u)
         launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias, true>,
-                      (unsigned)blocks, 256, p, stream);
+                      token_loop_layout(kLayout, true) ? blocks : norm_blocks, 256, p, stream);
     else
-        launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias, false>,
-                      (unsigned)blocks, 256, p, stream);
+        launch_kernel(kda_conv1d_update_kernel<kVec, kDtype, kLayout, kSilu, kBias, false>, blocks,
+                      256, p, stream);
 }
 
 template <int kDtype, int kLayout>
-void dispatch_update_act(const Params &p, int64_t blocks, bool silu, cudaStream_t s) {
+void dispatch_update_act(const Params &p, dim3 blocks, dim3 norm_blocks, bool silu,
+                         cudaStream_t s) {
     if (silu) {
         if (p.bias)
-            launch_update<kDtype, kLayout, true, true>(p, blocks, s);
+            launch_update<kDtype, kLayout, true, true>(p, blocks, norm_blocks, s);
         else
-            launch_update<kDtype, kLayout, true, false>(p, blocks, s);
+            launch_update<kDtype, kLayout, true, false>(p, blocks, norm_blocks, s);
     } else {
         if (p.bias)
-            launch_update<kDtype, kLayout, false, true>(p, blocks, s);
+            launch_update<kDtype, kLayout, false, true>(p, blocks, norm_blocks, s);
         else
-            launch_update<kDtype, kLayout, false, false>(p, blocks, s);
+            launch_update<kDtype, kLayout, false, false>(p, blocks, norm_blocks, s);
     }
 }
 
 // The decode step moves little besides the state lines, so a dense bf16 state
 // has its own lean variant (the general one holds about twice the registers).
+// Layouts 1, 3, 4 and 5 run a grid of about 4 CTAs per SM: in the token loop
+// blockIdx.x picks 256 channel vectors and blockIdx.y the first token, which
+// then steps by gridDim.y; otherwise a flat grid loops over the items.
 template <int kDtype>
 void dispatch_update(const Params &p, int64_t blocks, bool silu, cudaStream_t s) {
+    const int64_t nvec = p.dim / kVec;
+    const unsigned gx = (unsigned)((nvec + 255) / 256);
+    const int64_t resident = 4 * (int64_t)current_sms();
+    const int64_t want_y = resident / gx;
+    const unsigned gy = (unsigned)(want_y < 1 ? 1 : (want_y < p.tokens ? want_y : p.tokens));
+    const dim3 loop_grid(gx, gy);
+    const dim3 flat_loop((unsigned)(blocks < resident ? blocks : resident));
+    const dim3 flat((unsigned)blocks);
     if (p.weight_dense && p.state_dense)
         if (p.state_bf16)
-            dispatch_update_act<kDtype, 1>(
-                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
-                s);
+            dispatch_update_act<kDtype, 1>(p, loop_grid, flat_loop, silu, s);
         else
-            dispatch_update_act<kDtype, 0>(p, blocks, silu, s);
+            dispatch_update_act<kDtype, 0>(p, flat, flat, silu, s);
     else if ((p.weight_dense || p.weight_tapvec) && (p.state_dense || p.state_posvec))
         if (p.state_bf16)
-            dispatch_update_act<kDtype, 4>(
-                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
-                s);
+            dispatch_update_act<kDtype, 4>(p, loop_grid, flat_loop, silu, s);
         else if (p.state_posvec)
-            dispatch_update_act<kDtype, 3>(
-                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
-                s);
+            dispatch_update_act<kDtype, 3>(p, loop_grid, flat_loop, silu, s);
         else  // a dense fp32 state: the weight is tap-major (both dense is layout 0)
-            dispatch_update_act<kDtype, 5>(
-                p, blocks < 4 * (int64_t)current_sms() ? blocks : 4 * (int64_t)current_sms(), silu,
-                s);
+            dispatch_update_act<kDtype, 5>(p, loop_grid, flat_loop, silu, s);
     else
-        dispatch_update_act<kDtype, 2>(p, blocks, silu, s);
+        dispatch_update_act<kDtype, 2>(p, flat, flat, silu, s);
 }
 
 kda_status_t run_update(const void *x, int64_t x_row_stride, int64_t batch, int64_t dim,
