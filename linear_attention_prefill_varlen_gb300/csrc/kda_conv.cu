@@ -1425,7 +1425,7 @@ struct Shape {
 //   * One sequence: the smallest chunk for which every program fits in the
 //     budget at once, so no CTA waits for a later wave.
 //   * num_seqs at or above the budget's program count: the even spread of the
-//     tokens over the budget.
+//     tokens over the budget, no less than kSpreadFloor rows.
 //   * In between: the one-wave fit, but at most the even spread over two
 //     waves (no less than kSpreadFloor rows).  The one-wave fit alone gives
 //     tokens / (budget - num_seqs) rows, which grows without bound as num_seqs
@@ -1455,6 +1455,10 @@ Shape launch_shape(int64_t tokens, int64_t dim, int64_t num_seqs, int sms,
         }
     } else {
         chunk = (tokens * sh.warps_per_prog + slots - 1) / slots;
+        // no less than kSpreadFloor rows: fewer idle programs and a narrower
+        // search window for decode-sized batches (GB300: 1024 one-token
+        // sequences 29.7 -> 29.5 us, 1024 x 4 tokens 37.6 -> 37.3 us)
+        if (chunk < kSpreadFloor) chunk = kSpreadFloor;
     }
     chunk = (chunk + kQueue - 1) / kQueue * kQueue;
     if (chunk < kMinChunk) chunk = kMinChunk;
