@@ -14,10 +14,16 @@
 //     A program p belongs to sequence s with f(s) <= p < f(s+1),
 //     f(s) = floor(qsl[s] / chunk) + s: each sequence owns at least
 //     ceil(len / chunk) programs and there are ceil(tokens / chunk) + num_seqs
-//     in all (the bound the page's launch uses).  Each warp finds s by a
-//     radix-32 search over query_start_loc (one coalesced 32-candidate probe per
-//     level), so there is no host-side chunk table and the grid depends only on
-//     scalar sizes (graph-safe).
+//     in all (the bound the page's launch uses).  Each warp finds s on the
+//     device, by a radix-32 search over query_start_loc (one coalesced
+//     32-candidate probe per level) or, for batches of more than 32 sequences,
+//     by one round of loads over the window of query_start_loc that can hold
+//     the owner, so there is no host-side chunk table and the grid depends only
+//     on scalar sizes (graph-safe).
+//   * Batches of short sequences (under 16 rows on average) launch a separate
+//     instantiation with paths for programs shorter than the queue, one for
+//     single-row sequences (decode tokens), and an L2 prefetch of rows beyond
+//     the queue.
 //   * A thread owns VEC channels of its program's rows and walks them in order:
 //     3 history rows stay in registers as FP32, a rolling queue of P raw rows
 //     keeps P loads in flight (a slot is refilled as soon as its row has been
@@ -27,6 +33,11 @@
 //     thread, writes the updated state (the last rows of [old state ; the
 //     sequence's rows]), so each state line has exactly one reader and one
 //     writer and no ordering between CTAs is needed.
+//   * The decode-shaped update (one token per sequence) is its own kernel with
+//     no program search: one thread per (token, channel vector), or threads
+//     that keep a channel vector and loop over the tokens.
+//   * A device-side metadata check (two small kernels over the sequences)
+//     serves callers that want their metadata checked where it lives.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
