@@ -110,6 +110,20 @@ def profile_path(entry: str, workload: str) -> str:
     return os.path.join(PROFILES, f"{kernel}_{workload}{STORAGE_SUFFIX}.md")
 
 
+def packed_kernel_name(b: workloads.Batch) -> str:
+    """The kernel the timed call launches: the decode update, the looping
+    short kernel (at most one token per sequence, bf16/f16/fp32 x with a dense
+    fp32 width-3 state and a channel-major weight), or the conv kernel."""
+    if ENTRY == "update":
+        return "kda_conv1d_update_kernel"
+    default_state = (b.conv_states.dtype == np.float32 and b.conv_states.shape[2] == 3
+                     and LAYOUT_OPTS["state_layout"] == "dense"
+                     and LAYOUT_OPTS["weight_layout"] == "channel_major")
+    if b.tokens <= b.num_seqs and default_state:
+        return "kda_packed_conv1d_loop_kernel"
+    return "kda_packed_conv1d_kernel"
+
+
 def recorded_traffic(entry: str, workload: str) -> dict:
     """Per-launch DRAM bytes (read + write, and each side) recorded from one
     ncu capture in the committed summary of this kernel on this workload, if
@@ -808,8 +822,7 @@ def run_ours(args) -> None:
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      **recorded_traffic(ENTRY, b.name), "peak_source": peak_kind,
-                     "kernel": ("kda_conv1d_update_kernel" if ENTRY == "update"
-                                else "kda_packed_conv1d_kernel"),
+                     "kernel": packed_kernel_name(b),
                      "launch_us_mean": round(ms_per_step * 1e3, 3),
                      "launch_us_isolated_median": round(iso_median * 1e3, 3),
                      "launch_us_isolated_min": round(iso_min * 1e3, 3),

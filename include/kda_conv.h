@@ -318,8 +318,11 @@ kda_status_t kda_packed_conv1d_ex_check_args(
  * kda_packed_conv1d_launch_shape -- the launch kda_packed_conv1d makes for these
  * sizes on a GPU with sm_count SMs (sm_count = 0: the current device, which makes
  * one CUDA attribute query; a positive sm_count makes no CUDA call). *ctas = thread
- * blocks, *threads = threads per block, *chunk_tokens = tokens per program,
- * *programs = token programs (ceil(tokens/chunk) + num_seqs). Returns KDA_OK, or
+ * blocks of the program map, *threads = threads per block, *chunk_tokens = tokens
+ * per program, *programs = token programs (ceil(tokens/chunk) + num_seqs). A batch
+ * of at most one token per sequence (tokens <= num_seqs) in the default layout runs
+ * the map's blocks on at most one wave of resident blocks that loop over them; the
+ * launched grid is then min(*ctas, resident blocks). Returns KDA_OK, or
  * KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED for bad sizes. When tokens == 0 or
  * num_seqs == 0 all outputs are 0 (no launch). Output pointers may be NULL.
  */

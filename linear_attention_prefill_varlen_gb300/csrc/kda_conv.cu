@@ -23,7 +23,8 @@
 //   * Batches of short sequences (under 16 rows on average) launch a separate
 //     instantiation with paths for programs shorter than the queue, one for
 //     single-row sequences (decode tokens), and an L2 prefetch of rows beyond
-//     the queue.
+//     the queue.  Batches of at most one token per sequence run that code as
+//     one wave of resident blocks looping over the program map's blocks.
 //   * A thread owns VEC channels of its program's rows and walks them in order:
 //     3 history rows stay in registers as FP32, a rolling queue of P raw rows
 //     keeps P loads in flight (a slot is refilled as soon as its row has been
@@ -170,6 +171,7 @@ struct Params {
     uint32_t norm_mask;    // planes whose heads are L2-normalised (kNorm kernels)
     int norm_lanes;        // lanes per head: head_dim / VEC (a power of two <= 32)
     float norm_eps;        // added to the sum of squares inside the root
+    unsigned map_ctas;     // blocks of the program map (total_warps / warps per block)
 };
 
 // ---------------------------------------------------------------------------
@@ -653,23 +655,17 @@ __host__ __device__ constexpr int min_blocks() {
 // 256 short prefills + 1024 decode tokens).  A single wave of long chunks
 // already saturates DRAM: there the same prefetch cost 8-12 %.
 // kNorm: planes in norm_mask get the per-head L2 norm after the activation.
+// conv_block runs the warps of block `block` of the program map: map warp
+// block * (blockDim.x / 32) + threadIdx.x / 32.
 template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias,
           bool kShort, bool kNorm>
-__global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>()))
-    kda_packed_conv1d_kernel(const Params p) {
-#if KDA_PDL
-    // Launched as a programmatic dependent: wait until the preceding grid in
-    // the stream has completed and its writes are visible (the same order a
-    // plain launch gives), and let the next grid be scheduled meanwhile.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" :::);
-#endif
+__device__ __forceinline__ void conv_block(const Params &p, const unsigned block) {
     constexpr int W = row_words<VEC, kDtype>();
     // x and out are addressed in elements of their storage type
     using XT = typename std::conditional<kDtype == KDA_DTYPE_F32, float, uint16_t>::type;
     using OT = typename std::conditional<kPreact, float, XT>::type;
     const int lane = threadIdx.x & 31;
-    const int64_t gwarp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t gwarp = (int64_t)block * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (gwarp >= p.total_warps) return;  // whole warps only
     const int prog = (int)fast_div((uint32_t)gwarp, p.wpp_div);  // total_warps < 2^32
     const int wv = (int)(gwarp - (int64_t)prog * p.warps_per_prog);
@@ -989,6 +985,41 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
     }
     for (; t + 2 * P <= t1; t += P) rows(std::false_type{});
     for (; t < t1; t += P) rows(std::true_type{});
+}
+
+// Launched as a programmatic dependent: wait until the preceding grid in the
+// stream has completed and its writes are visible (the same order a plain
+// launch gives), and let the next grid be scheduled meanwhile.
+__device__ __forceinline__ void pdl_prologue() {
+#if KDA_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+#endif
+}
+
+template <int VEC, int P, int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias,
+          bool kShort, bool kNorm>
+__global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>()))
+    kda_packed_conv1d_kernel(const Params p) {
+    pdl_prologue();
+    conv_block<VEC, P, kDtype, kGeneral, kPreact, kSilu, kBias, kShort, kNorm>(p, blockIdx.x);
+}
+
+// Batches of at most one token per sequence (decode steps): one wave of
+// resident blocks, each looping over the blocks of the program map in
+// round-robin order.  A warp starts its next one-token program as soon as it
+// finishes, with no block launch or retirement in between (GB300, 1024
+// one-token sequences: 29.9 -> 27.4 us).  A separate instantiation: compiled
+// into the short kernel itself, the loop made its row path spill 12-16 bytes
+// and cost 4 % on 1024 x 4 tokens; and for batches that mix 1-row and 48-row
+// programs a round-robin assignment cannot balance the load as the block
+// scheduler does (256 short prefills + 1024 decode tokens 78.9 -> 104.4 us).
+template <int VEC, int P, int kDtype, bool kSilu, bool kBias, bool kNorm>
+__global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>()))
+    kda_packed_conv1d_loop_kernel(const Params p) {
+    pdl_prologue();
+    for (unsigned b = blockIdx.x; b < p.map_ctas; b += gridDim.x)
+        conv_block<VEC, P, kDtype, false, false, kSilu, kBias, true, kNorm>(p, b);
 }
 
 // The epilogue alone, over consecutive fp32 bit patterns, VEC at a time
@@ -1528,14 +1559,24 @@ void launch_kernel(void (*kernel)(Params), dim3 blocks, unsigned threads, const 
 
 template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias, bool kNorm>
 void launch_norm(const Params &p, const Shape &sh, cudaStream_t stream) {
-    if (sh.short_seqs)
+    if (sh.short_seqs) {
+        if constexpr (!kGeneral && !kPreact) {
+            if (p.tokens <= p.num_seqs) {  // at most one token per sequence on average
+                const int64_t resident = (int64_t)current_sms() * min_blocks<kDtype, kNorm>();
+                launch_kernel(kda_packed_conv1d_loop_kernel<kVec, kQueue, kDtype, kSilu, kBias, kNorm>,
+                              dim3((unsigned)std::min(sh.ctas, resident)), (unsigned)sh.threads, p,
+                              stream);
+                return;
+            }
+        }
         launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu,
                                                kBias, true, kNorm>,
                       dim3((unsigned)sh.ctas), (unsigned)sh.threads, p, stream);
-    else
+    } else {
         launch_kernel(kda_packed_conv1d_kernel<kVec, kQueue, kDtype, kGeneral, kPreact, kSilu,
                                                kBias, false, kNorm>,
                       dim3((unsigned)sh.ctas), (unsigned)sh.threads, p, stream);
+    }
 }
 
 template <int kDtype, bool kGeneral, bool kPreact, bool kSilu, bool kBias>
@@ -1672,6 +1713,7 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     p.wpp_div = make_fast_div((uint32_t)sh.warps_per_prog);
     p.part_div = make_fast_div((uint32_t)part_dim);
     p.total_warps = sh.total_warps;
+    p.map_ctas = (unsigned)sh.ctas;
     int steps = 0;
     int64_t reach = 1;
     while (reach < num_seqs) {

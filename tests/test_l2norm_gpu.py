@@ -110,6 +110,9 @@ CASES = [
     ("bf16_h16_nobias", 1106, [12, 1, 33], 192, 64, 200, 8, 0b110, 16, {"bias_std": None}),
     ("f16_k5_h128", 1107, [2, 6, 20], 512, 256, 520, 8, 0b11, 128,
      {"x_dtype": "f16", "state_width": 5}),
+    # at most one token per sequence: the looping short kernel with the norm
+    ("bf16_h128_one_token", 1108, [1] * 40 + [0] * 6 + [2] * 3, 768, 256, 776, 8, 0b011, 128,
+     {}),
 ]
 
 

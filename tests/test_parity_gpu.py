@@ -107,6 +107,14 @@ SWEEP = [
     # programs both shorter and longer than the queue
     (209, [1, 2, 3, 4, 5, 6, 7, 8, 9, 13, 1, 1, 1, 1, 1, 1], 256, 128, 264, 8, {"his_p": 0.5}),
     (210, [0, 5, 0, 1, 2, 0, 4], 192, 64, 200, 8, {"activation": 0}),
+    # at most one token per sequence (tokens <= num_seqs): the looping short
+    # kernel.  Empty, one- and few-row sequences; one sequence longer than two
+    # chunks beside empty ones; and a map of more blocks than one wave holds,
+    # so that resident blocks loop over several
+    (211, [0, 1, 0, 3, 1, 0, 1, 2, 0, 0, 1, 1, 0, 1], 256, 128, 264, 8,
+     {"his_p": 0.5, "null_count": 2}),
+    (212, [130] + [0] * 129 + [1] * 20, 192, 64, 200, 8, {"his_p": 0.7}),
+    (213, ([1] * 25 + [0] * 4 + [2]) * 100, 256, 128, 264, 8, {"null_count": 40}),
 ]
 
 
@@ -198,6 +206,40 @@ def test_cuda_graph_replay_with_new_metadata():
     with torch.cuda.graph(g, stream=stream):
         d.run(torch.cuda.current_stream())
     for b in (b1, b2):
+        d.conv_states.copy_(torch.from_numpy(b.conv_states))
+        d.query_start_loc.copy_(torch.from_numpy(b.query_start_loc))
+        d.cache_indices.copy_(torch.from_numpy(b.cache_indices))
+        d.has_initial_state.copy_(torch.from_numpy(b.has_initial_state))
+        d.out.fill_(-1)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ref, ref_states = oracle_run(b)
+        assert_states_equal(d.states(), ref_states)
+        assert_outputs_match(d.out_bits(), ref["out"], b.activation)
+
+
+def test_cuda_graph_replay_one_token_batch():
+    """The looping short kernel (at most one token per sequence) captured once
+    and replayed with new lengths, cache lines and initial-state flags."""
+    b1 = pins.small_batch(305, [1] * 50 + [0] * 10, dim=256, part_dim=128, null_count=3,
+                          cache_lines=70)
+    assert b1.tokens <= b1.num_seqs
+    b2 = b1.copy()
+    lengths = np.array([2, 0, 3] + [1] * 45 + [0] * 12)  # same tokens (50), same num_seqs
+    assert lengths.sum() == b1.tokens and lengths.size == b1.num_seqs
+    b2.query_start_loc = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    b2.cache_indices = np.random.default_rng(11).permutation(70)[:60].astype(np.int32)
+    b2.cache_indices[[4, 9]] = -1
+    b2.has_initial_state = (np.arange(60) % 3 != 0).astype(np.uint8)
+    d = DeviceBatch(b1)
+    stream = torch.cuda.Stream()
+    d.run(stream)  # warm-up outside capture
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        d.run(torch.cuda.current_stream())
+    for b in (b1, b2, b1):
         d.conv_states.copy_(torch.from_numpy(b.conv_states))
         d.query_start_loc.copy_(torch.from_numpy(b.query_start_loc))
         d.cache_indices.copy_(torch.from_numpy(b.cache_indices))
