@@ -103,3 +103,26 @@ def test_prepared_step_matches_the_c_signature(entry, norm, layout):
         bench.ENTRY, bench.NORM = old[0], old[1]
         bench.LAYOUT_OPTS.clear()
         bench.LAYOUT_OPTS.update(old[2])
+
+
+def test_sized_workload_names():
+    """prefill<T> / decode<N> build the 16K chunk's and the decode step's
+    shapes at other sizes; other names are rejected by the option parser."""
+    import bench
+    import workloads
+
+    b = workloads.by_name("prefill4096")
+    assert (b.tokens, b.num_seqs, b.dim, b.part_dim, b.row_stride) == (4096, 1, 4608, 1536, 6400)
+    d = workloads.by_name("decode256")
+    assert (d.tokens, d.num_seqs) == (256, 256) and d.conv_states.shape[0] == 512
+    assert workloads.by_name("long16k").name == "long16k"
+    for bad in ("prefill0", "prefill", "decode-1", "long8k", "prefill12345678"):
+        assert not workloads.valid_name(bad)
+        with pytest.raises(SystemExit):
+            bench.parse_args(["--workload", bad])
+    assert bench.parse_args(["--workload", "decode4096"]).workload == "decode4096"
+    # the page's figure covers 2K-16K-token prefill chunks
+    assert bench.page_range(workloads.by_name("prefill2048"))
+    assert bench.page_range(b)
+    assert not bench.page_range(workloads.by_name("prefill32768"))
+    assert not bench.page_range(d)

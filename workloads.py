@@ -34,6 +34,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass, field
 
+import re
+
 import numpy as np
 import torch
 
@@ -222,6 +224,36 @@ WORKLOADS = {
     "spec_decode": spec_decode,
     "skewed": skewed,
 }
+
+
+def prefill(tokens: int, **kw) -> Batch:
+    """One prefill sequence of `tokens` tokens, otherwise the 16K chunk's shape
+    (3 x 1536 channels, row stride 6400, an initial state, 8 cache lines)."""
+    return make_batch(f"prefill{tokens}", 2, [tokens], 4608, 1536, 6400, 8, his=[1], **kw)
+
+
+def decode_batch(n: int, **kw) -> Batch:
+    """n sequences of one token each (a decode step), 2n cache lines."""
+    return make_batch(f"decode{n}", 5, [1] * n, 4608, 1536, 6400, 2 * n, his_p=1.0, **kw)
+
+
+_SIZED = re.compile(r"(prefill|decode)([1-9][0-9]{0,6})")
+
+
+def valid_name(name: str) -> bool:
+    return name in WORKLOADS or _SIZED.fullmatch(name) is not None
+
+
+def by_name(name: str, **kw) -> Batch:
+    """A workload of WORKLOADS, or prefill<T> / decode<N> at any size (for
+    size sweeps; the same draws as long16k / decode at their own sizes)."""
+    if name in WORKLOADS:
+        return WORKLOADS[name](**kw)
+    m = _SIZED.fullmatch(name)
+    if m is None:
+        raise KeyError(name)
+    n = int(m.group(2))
+    return prefill(n, **kw) if m.group(1) == "prefill" else decode_batch(n, **kw)
 
 
 def algorithmic_bytes(b: Batch) -> int:
