@@ -288,6 +288,27 @@ def test_many_sequences_four_search_levels():
     assert_outputs_match(d.out_bits(), ref["out"], b.activation)
 
 
+def test_many_one_token_sequences_radix_search_in_the_loop():
+    """40,000 sequences of 0, 1 or 2 tokens with no more tokens than
+    sequences: the looping short kernel, whose window would be too wide, so
+    each block finds its sequence by the four-level radix search."""
+    rng = np.random.default_rng(8)
+    lengths = rng.integers(0, 3, size=40000)
+    twos = np.flatnonzero(lengths == 2)
+    excess = int(lengths.sum()) - lengths.size
+    if excess > 0:
+        lengths[rng.choice(twos, size=excess, replace=False)] = 1
+    assert lengths.sum() <= lengths.size
+    b = workloads.make_batch("many_one_token", 702, lengths.tolist(), 64, 64, 64, 40010,
+                             his_p=0.5, null_count=500)
+    ref, ref_states = oracle_run(b)
+    d = DeviceBatch(b)
+    d.run()
+    torch.cuda.synchronize()
+    assert_states_equal(d.states(), ref_states)
+    assert_outputs_match(d.out_bits(), ref["out"], b.activation)
+
+
 def test_short_batch_prefetch_on_a_half_warp_segment():
     """A batch of short sequences (mean 14.3 rows: the short instantiation)
     large enough for 24-row chunks, so its steps issue the L2 prefetch of
