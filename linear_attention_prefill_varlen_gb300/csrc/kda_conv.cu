@@ -633,13 +633,36 @@ __device__ __forceinline__ void l2_prefetch(const void *ptr, uint32_t bytes) {
 
 // Resident CTAs per SM the register budget is sized for: fp32 rows are twice
 // as wide, so their queue needs more registers.  The L2-norm epilogue holds a
-// whole step's activations at once (its P head reductions run side by side),
-// which costs two CTAs.  Measured on GB300 for the 16K prefill with the norm:
-// 6 CTAs and one row at a time 68.5 us, 5 CTAs and all P rows 59.1 us (56.8 us
-// with the reduce-scatter form for 128-channel heads).
+// whole step's activations at once (its P head reductions run side by side,
+// 24 more registers); it pays for them by keeping the thread's taps and bias
+// in shared memory instead (reloaded per row, 20 registers fewer), so it runs
+// at the plain kernel's occupancy.  Measured on GB300 for the 16K prefill with
+// the norm: taps in registers at 5 CTAs 58.2 us, in shared memory at 7 CTAs
+// 53.9 us (the plain kernel 52.6 us in the same process); 256 short prefills +
+// 1024 decode tokens 94.5 -> 83.8 us; 64-channel heads (4 x 8192 tokens x
+// 3 x 1088) 82.0 -> 73.8 us.
+// fp32 x keeps two CTAs fewer with the norm: at the plain fp32 budget its
+// norm variants spill.
 template <int kDtype, bool kNorm = false>
 __host__ __device__ constexpr int min_blocks() {
-    return (kDtype == KDA_DTYPE_F32 ? KDA_MIN_BLOCKS_F32 : KDA_MIN_BLOCKS) - (kNorm ? 2 : 0);
+    return kDtype == KDA_DTYPE_F32 ? KDA_MIN_BLOCKS_F32 - (kNorm ? 2 : 0) : KDA_MIN_BLOCKS;
+}
+
+// This thread's taps (VEC float4) and bias (VEC / 4 float4) from shared
+// address a, loaded afresh at each use (volatile: kept next to the use).
+template <int VEC>
+__device__ __forceinline__ void taps_from_shared(uint32_t a, float (&w)[VEC][4],
+                                                 float (&b)[VEC]) {
+#pragma unroll
+    for (int v = 0; v < VEC; ++v)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(w[v][0]), "=f"(w[v][1]), "=f"(w[v][2]), "=f"(w[v][3])
+                     : "r"(a + 16u * v));
+#pragma unroll
+    for (int i = 0; i < VEC / 4; ++i)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(b[4 * i]), "=f"(b[4 * i + 1]), "=f"(b[4 * i + 2]), "=f"(b[4 * i + 3])
+                     : "r"(a + 16u * (VEC + i)));
 }
 
 // kGeneral: the weight and the conv state may have any strides and the state
@@ -777,6 +800,22 @@ __device__ __forceinline__ void conv_block(const Params &p, const unsigned block
             return;
         }
     }
+    // kNorm: the taps and bias move to this thread's slot of shared memory
+    // and are reloaded for each row (see min_blocks).  Only the thread itself
+    // reads its slot, so no barrier is needed.
+    uint32_t tap_slot = 0;
+    if constexpr (kNorm) {
+        static_assert(VEC % 4 == 0, "taps and bias as float4s");
+        __shared__ __align__(16) float4 taps_smem[KDA_CTA_THREADS][VEC + VEC / 4];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v)
+            taps_smem[threadIdx.x][v] = make_float4(w[v][0], w[v][1], w[v][2], w[v][3]);
+#pragma unroll
+        for (int i = 0; i < VEC / 4; ++i)
+            taps_smem[threadIdx.x][VEC + i] =
+                make_float4(bias[4 * i], bias[4 * i + 1], bias[4 * i + 2], bias[4 * i + 3]);
+        tap_slot = (uint32_t)__cvta_generic_to_shared(&taps_smem[threadIdx.x][0]);
+    }
     // Register queue: slot u holds row t+u; it is refilled with row t+P+u as
     // soon as row t+u has been widened, so P rows are always in flight.
     uint32_t q[P][W];
@@ -881,6 +920,17 @@ __device__ __forceinline__ void conv_block(const Params &p, const unsigned block
         widen<VEC, kDtype>(raw, h2);
     }
 
+    // One row's taps, from registers or (kNorm) from the shared slot.
+    auto row_taps = [&](const float (&xv)[VEC], float (&yy)[VEC]) {
+        if constexpr (kNorm) {
+            float wr[VEC][4], br[VEC];
+            taps_from_shared<VEC>(tap_slot, wr, br);
+            taps_row<VEC, kBias>(wr, br, h0, h1, h2, xv, yy);
+        } else {
+            taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, yy);
+        }
+    };
+
     const int plane = (int)fast_div((uint32_t)c, p.part_div);
     const int col = c - plane * p.part_dim;
     const int64_t out_row = p.part_dim;  // elements between output rows
@@ -904,7 +954,7 @@ __device__ __forceinline__ void conv_block(const Params &p, const unsigned block
                 float xv[VEC];
                 widen<VEC, kDtype>(q[u], xv);
                 if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
-                taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y[u]);
+                row_taps(xv, y[u]);
                 if constexpr (kSilu) silu_row<VEC>(y[u]);
             }
             if (norm_on) {
@@ -934,7 +984,7 @@ __device__ __forceinline__ void conv_block(const Params &p, const unsigned block
                 widen<VEC, kDtype>(q[u], xv);
                 if (!kChecked || t + P + u < t1) load_row<W>(xnext + (int64_t)u * xs, q[u]);
                 float y[VEC];
-                taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);
+                row_taps(xv, y);
                 if constexpr (kSilu) silu_row<VEC>(y);
                 if (!kChecked || t + u < t1) {
                     OT *dst = static_cast<OT *>(p.out) + o + u * out_row;
@@ -959,7 +1009,7 @@ __device__ __forceinline__ void conv_block(const Params &p, const unsigned block
                 float xv[VEC];
                 widen<VEC, kDtype>(q[u], xv);
                 float y[VEC];
-                taps_row<VEC, kBias>(w, bias, h0, h1, h2, xv, y);
+                row_taps(xv, y);
                 if constexpr (kSilu) silu_row<VEC>(y);
                 if constexpr (kNorm) {
                     if (norm_on) l2norm_row<VEC>(y, p.norm_eps, p.norm_lanes, norm_group);
@@ -1674,9 +1724,10 @@ kda_status_t run(const void *x, int64_t x_row_stride, int64_t tokens, int64_t di
     if (tokens == 0 || num_seqs == 0 || dim == 0) return KDA_OK;
 
     const bool norm_on = !preact && norm && norm->plane_mask != 0u;
-    const int blocks_per_sm =
-        (l.x_dtype == KDA_DTYPE_F32 ? min_blocks<KDA_DTYPE_F32>() : min_blocks<KDA_DTYPE_BF16>()) -
-        (norm_on ? 2 : 0);
+    const int blocks_per_sm = l.x_dtype == KDA_DTYPE_F32
+                                  ? (norm_on ? min_blocks<KDA_DTYPE_F32, true>()
+                                             : min_blocks<KDA_DTYPE_F32>())
+                                  : min_blocks<KDA_DTYPE_BF16>();
     const Shape sh = launch_shape(tokens, dim, num_seqs, current_sms(), blocks_per_sm);
     // warp and program indices are divided in 32 bits on the device
     if (sh.ctas > INT32_MAX || sh.total_warps >= (int64_t(1) << 32)) return KDA_ERR_INVALID_ARG;
