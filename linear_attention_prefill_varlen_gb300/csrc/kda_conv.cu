@@ -70,6 +70,12 @@
 #ifndef KDA_MIN_BLOCKS_F32
 #define KDA_MIN_BLOCKS_F32 5  // the same for fp32 x (twice the queue registers)
 #endif
+#ifndef KDA_LOOP_MIN_BLOCKS
+#define KDA_LOOP_MIN_BLOCKS 8  // the looping one-token kernel (16-bit x, no norm)
+#endif
+#ifndef KDA_LOOP_QUEUE
+#define KDA_LOOP_QUEUE 3  // its queue depth for the rare programs of several rows
+#endif
 #ifndef KDA_WAVES
 #define KDA_WAVES 1  // waves of resident warps a long prefill is spread over
 #endif
@@ -1064,8 +1070,20 @@ __global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>())
 // and cost 4 % on 1024 x 4 tokens; and for batches that mix 1-row and 48-row
 // programs a round-robin assignment cannot balance the load as the block
 // scheduler does (256 short prefills + 1024 decode tokens 78.9 -> 104.4 us).
+// For 16-bit x without the norm it runs 8 blocks per SM, its programs of
+// several rows (rare in such batches) taking a 3-row queue (P): against 7
+// blocks and 6 rows, 1024 one-token sequences 27.3 -> 26.9 us, 4096 96.9 ->
+// 94.4 us, 256 10.4 -> 9.3 us.
+template <int kDtype, bool kNorm>
+__host__ __device__ constexpr bool loop_lean() {
+    return !kNorm && kDtype != KDA_DTYPE_F32;
+}
+template <int kDtype, bool kNorm>
+__host__ __device__ constexpr int loop_blocks() {
+    return loop_lean<kDtype, kNorm>() ? KDA_LOOP_MIN_BLOCKS : min_blocks<kDtype, kNorm>();
+}
 template <int VEC, int P, int kDtype, bool kSilu, bool kBias, bool kNorm>
-__global__ void __launch_bounds__(KDA_CTA_THREADS, (min_blocks<kDtype, kNorm>()))
+__global__ void __launch_bounds__(KDA_CTA_THREADS, (loop_blocks<kDtype, kNorm>()))
     kda_packed_conv1d_loop_kernel(const Params p) {
     pdl_prologue();
     for (unsigned b = blockIdx.x; b < p.map_ctas; b += gridDim.x)
@@ -1612,8 +1630,9 @@ void launch_norm(const Params &p, const Shape &sh, cudaStream_t stream) {
     if (sh.short_seqs) {
         if constexpr (!kGeneral && !kPreact) {
             if (p.tokens <= p.num_seqs) {  // at most one token per sequence on average
-                const int64_t resident = (int64_t)current_sms() * min_blocks<kDtype, kNorm>();
-                launch_kernel(kda_packed_conv1d_loop_kernel<kVec, kQueue, kDtype, kSilu, kBias, kNorm>,
+                const int64_t resident = (int64_t)current_sms() * loop_blocks<kDtype, kNorm>();
+                constexpr int kLoopP = loop_lean<kDtype, kNorm>() ? KDA_LOOP_QUEUE : kQueue;
+                launch_kernel(kda_packed_conv1d_loop_kernel<kVec, kLoopP, kDtype, kSilu, kBias, kNorm>,
                               dim3((unsigned)std::min(sh.ctas, resident)), (unsigned)sh.threads, p,
                               stream);
                 return;
