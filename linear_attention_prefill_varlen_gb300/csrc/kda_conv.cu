@@ -821,6 +821,10 @@ __device__ __forceinline__ void conv_block(const Params &p, const unsigned block
             taps_smem[threadIdx.x][VEC + i] =
                 make_float4(bias[4 * i], bias[4 * i + 1], bias[4 * i + 2], bias[4 * i + 3]);
         tap_slot = (uint32_t)__cvta_generic_to_shared(&taps_smem[threadIdx.x][0]);
+        // the reloads are asm the compiler cannot see into: keep the stores
+        // above them (a compiler-only barrier; one thread, one address, so
+        // the hardware keeps the order)
+        asm volatile("" ::: "memory");
     }
     // Register queue: slot u holds row t+u; it is refilled with row t+P+u as
     // soon as row t+u has been widened, so P rows are always in flight.
